@@ -1,0 +1,448 @@
+"""Benchmark of the exact-attention forward path on GB300.
+
+One timed step is one forward pass of causal prefill attention over the workload the headline
+metric is quoted on (B=4, Hq=Hkv=32, S=4096, d=128, bf16, synthetic N(0,1) inputs). The same run
+also times, with the same step and warm-up counts, the other workloads of the hot path: long-context
+GQA prefill (S=32768), paged ragged prefill (64 sequences) and paged split-KV decode (128
+sequences); their numbers go to the "extra" object of the single JSON line rank 0 prints.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this project has) on a bounded
+sample of the same workload. Under torchrun every rank runs the same per-GPU work (weak scaling,
+no collective on the data path); rank 0 reports the whole-job throughput over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from io_aware_exact_flash_gb300.workloads import (  # noqa: E402
+    WORKLOADS,
+    make_dense,
+    make_paged,
+    paged_allowed_scores,
+)
+
+METRIC = "attn fwd TFLOP/s (prefill) & decode HBM GB/s on 1 GB300, % of roofline"
+HEADLINE = "causal_prefill_b4_h32_s4096_d128"
+EXTRAS = ["gqa_causal_prefill_b1_hq32_hkv8_s32768_d128", "paged_prefill_64seq_512_8192_hq32_hkv8_d128_p16",
+          "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ----------------------------------------------------------------------------- distributed glue
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (x itself with one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- peaks and clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                raw = json.load(f)
+
+            def pick(*names):
+                for n in names:
+                    for k, v in raw.items():
+                        if k == n and isinstance(v, (int, float)):
+                            return float(v)
+                return None
+
+            peaks = {"hbm_gbs": pick("hbm_gbs"), "bf16_tflops": pick("bf16_tflops"),
+                     "bf16_tflops_sustained": pick("bf16_tflops_sustained")}
+            if all(v is not None for v in peaks.values()):
+                peaks["source"] = "measured"
+                return peaks
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            text, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(text)):
+            if len(row) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads on device
+def to_dev(bits, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def i32(a, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+class DenseCase:
+    def __init__(self, name, device):
+        import torch
+
+        self.w = WORKLOADS[name]
+        t = make_dense(self.w)
+        self.host = t
+        self.q, self.k, self.v = (to_dev(t[x], device) for x in ("q", "k", "v"))
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=device)
+        self.flops = self.w.flops()
+        self.kind = "prefill"
+
+    def run(self):
+        import io_aware_exact_flash_gb300 as fa
+
+        fa.fa_fwd(self.q, self.k, self.v, causal=self.w.causal, scale=self.w.scale, out=self.o, lse=self.lse)
+
+    launches = 1
+
+
+class PagedCase:
+    def __init__(self, name, device):
+        import torch
+
+        import io_aware_exact_flash_gb300 as fa
+
+        self.w = WORKLOADS[name]
+        t = make_paged(self.w)
+        self.host = t
+        self.q = to_dev(t["q"], device)
+        self.kp, self.vp = to_dev(t["k_pages"], device), to_dev(t["v_pages"], device)
+        self.pt, self.cu, self.kl = i32(t["page_table"], device), i32(t["cu_seqlens_q"], device), i32(t["kv_lens"], device)
+        self.max_q = int(t["q_lens"].max())
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
+        need = fa.fa_paged_workspace_bytes(self.w.num_seqs, t["total_q"], self.max_q, self.w.page_size,
+                                           t["page_table"].shape[1], t["num_pages"], self.w.Hq, self.w.Hkv, self.w.d)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.scores = paged_allowed_scores(t, self.w.Hq, self.w.causal)
+        self.flops = 4.0 * self.w.d * self.scores
+        self.kind = "decode" if self.w.decode else "prefill"
+        # algorithmic bytes of decode: every K and V row read once, q read, o and lse written
+        kv_rows = int(t["kv_lens"].astype(np.int64).sum())
+        self.bytes = (2 * kv_rows * self.w.Hkv * self.w.d * 2 + t["total_q"] * self.w.Hq * self.w.d * 2 * 2
+                      + t["total_q"] * self.w.Hq * 4)
+        if self.w.decode:
+            self.splits = fa.fa_decode_num_splits(self.w.num_seqs, self.w.page_size, t["page_table"].shape[1],
+                                                  t["num_pages"], self.w.Hkv)
+        else:
+            self.splits = 1
+
+    def run(self):
+        import io_aware_exact_flash_gb300 as fa
+
+        fa.fa_paged_fwd(self.q, self.kp, self.vp, self.pt, self.cu, self.kl, self.max_q, causal=self.w.causal,
+                        scale=self.w.scale, out=self.o, lse=self.lse, workspace=self.ws)
+
+    @property
+    def launches(self):
+        return 2 if (not self.w.decode or self.splits > 1) else 1
+
+
+def time_case(case, steps, warmup, flush):
+    """Per-step device time (ms) of case.run() with CUDA events on the launching stream; L2 is
+    flushed before every step, outside the timed interval."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        case.run()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        case.run()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def e2e_dense(case, steps, warmup, device):
+    """Headline metric through the public API with host buffers: every step copies q, k, v from
+    pinned host memory, runs the forward and copies O and LSE back."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    hq, hk, hv = (case.q.cpu().pin_memory(), case.k.cpu().pin_memory(), case.v.cpu().pin_memory())
+    ho = torch.empty(case.o.shape, dtype=case.o.dtype).pin_memory()
+    hl = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        o, lse = fa.fa_fwd(dq, dk, dv, causal=case.w.causal, scale=case.w.scale, out=case.o, lse=case.lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return ms, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, t, target_s=12.0, seed=0):
+    """Times the fp64 oracle, as it stands, on a bounded random sample of query rows of the dense
+    workload; returns (TFLOP/s, sample description, threads)."""
+    import oracle
+
+    orc = oracle.get()
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+
+    def rows_for(n):
+        b = rng.integers(0, w.B, n)
+        i = rng.integers(0, w.S, n)
+        h = rng.integers(0, w.Hq, n)
+        return np.stack([b, i, h], axis=1).astype(np.int64)
+
+    def flops_of(rows):
+        n_keys = rows[:, 1] + 1 if w.causal else np.full(len(rows), w.S)
+        return 4.0 * w.d * float(n_keys.sum())
+
+    probe = rows_for(max(threads, 64))
+    t0 = time.perf_counter()
+    orc.dense_rows(t["q"], t["k"], t["v"], w.causal, w.scale, probe, threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(200000, max(threads, len(probe) * target_s / dt)))
+    rows = rows_for(n)
+    t0 = time.perf_counter()
+    orc.dense_rows(t["q"], t["k"], t["v"], w.causal, w.scale, rows, threads)
+    dt = time.perf_counter() - t0
+    return flops_of(rows) / dt / 1e12, f"{n} random (b, i, h) query rows of {w.name}, {dt:.1f} s", threads
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle on the same workload, metric and unit."""
+    if rank != 0:
+        return 0
+    w = WORKLOADS[HEADLINE]
+    t = make_dense(w)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    desc, threads = "", 1
+    for i in range(args.warmup + args.steps):
+        v, desc, threads = oracle_sample(w, t, target_s=per_step, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "causal": True},
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "TFLOP/s", "cores": threads,
+                             "sample": desc + " per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--extras", default="all", help="comma list of extra workloads, 'all' or 'none'")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+
+    dist_init(world, "nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import io_aware_exact_flash_gb300 as fa
+
+    fa.load_library()
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    head = DenseCase(HEADLINE, device)
+    extra_names = EXTRAS if args.extras == "all" else ([] if args.extras == "none" else args.extras.split(","))
+    extras = [(n, (PagedCase if n.startswith("paged") else DenseCase)(n, device)) for n in extra_names]
+
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    head_ms = time_case(head, args.steps, args.warmup, flush)
+    extra_ms = {n: time_case(c, args.steps, args.warmup, flush) for n, c in extras}
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    barrier(world)
+    clocks = sampler.stop()
+    code, site = fa.fa_get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {site}")
+
+    mean_ms = max_over_ranks(statistics.mean(head_ms), world, device)
+    value = world * head.flops / (mean_ms * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = e2e_dense(head, max(3, args.steps // 2), 3, device)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_value = world * head.flops / (e2e_ms * 1e-3) / 1e12
+
+    peak_t = peaks["bf16_tflops"]
+    label = "of measured" if peaks["source"] == "measured" else "of fallback"
+    roof = {"bound": "tensor", "achieved": head.flops / (statistics.mean(head_ms) * 1e-3) / 1e12, "peak": peak_t,
+            "unit": "TFLOP/s", "frac": None, "traffic": None, "peak_source": label,
+            "kernel": "prefill_kernel<128,false>", "per_launch_flops": head.flops}
+    roof["frac"] = roof["achieved"] / peak_t
+
+    extra = {}
+    for n, c in extras:
+        ms = statistics.mean(extra_ms[n])
+        if c.kind == "decode":
+            gbs = c.bytes / (ms * 1e-3) / 1e9
+            extra[n] = {"metric": "decode HBM GB/s", "value": gbs, "unit": "GB/s", "ms": ms,
+                        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": gbs / peaks["hbm_gbs"], "peak_source": label,
+                                     "per_launch_bytes": c.bytes},
+                        "splits": c.splits}
+        else:
+            tf = c.flops / (ms * 1e-3) / 1e12
+            extra[n] = {"metric": "prefill TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms": ms,
+                        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_t, "unit": "TFLOP/s",
+                                     "frac": tf / peak_t, "peak_source": label, "per_launch_flops": c.flops}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, threads = oracle_sample(head.w, head.host, target_s=12.0)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    launches = args.steps * (head.launches + sum(c.launches for _, c in extras))
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": HEADLINE, "B": head.w.B, "S": head.w.S, "Hq": head.w.Hq, "Hkv": head.w.Hkv,
+                           "d": head.w.d, "causal": True, "parallelism": f"replicas x{world}",
+                           "l2": "flushed before every timed step (512 MB write)"},
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "clocks": clocks, "timed_wall_s": wall, "extra": extra}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,126 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention forward library.
+ *
+ * What is computed (all entry points): for every query row i and query head h,
+ *     O[i,h,:] = softmax_j( scale * q_i . k_j  over the keys j that row i may attend to ) . V
+ *     LSE[i,h] = ln sum_j exp(scale * q_i . k_j)      (same key set)
+ * This is the naive pipeline of "I/O-Aware Kernels" (datasystem.school, Module 5), section
+ * "Naive attention: materializing the k x k score matrix", computed instead the way its section
+ * "FlashAttention: tiling + online softmax" describes: one query tile stays on chip while key and
+ * value tiles stream past it, with a running row maximum m and sum l and a rescaled output
+ * accumulator, so the score matrix never reaches device memory. The paged entry point is the
+ * serving form of its section "FlashInfer: I/O-aware attention for serving": keys and values are
+ * gathered from a paged cache through a page table, over a ragged batch, with grouped-query heads.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are bf16 (IEEE binary16-brain, passed as void*), contiguous, innermost dimension
+ *    last. LSE is fp32. Accumulation is fp32; P is rounded to bf16 before P.V.
+ *  - Grouped-query heads: query head h reads key/value head h / (Hq / Hkv); Hq % Hkv must be 0.
+ *  - causal != 0 masks bottom-right aligned: row i of a sequence with q_len query rows and kv_len
+ *    keys attends to key j iff j <= i + (kv_len - q_len). A row with no key gets O = 0 and
+ *    LSE = -inf.
+ *  - Supported head dims: d = 64 and d = 128. Every pointer must be 16-byte aligned.
+ *  - Memory: the caller owns all device memory (inputs, outputs, workspace). The library never
+ *    allocates or frees device memory. Its only global state is one device status word per GPU
+ *    (see fa_get_device_status) and a cached driver entry point.
+ *  - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *    FA_OK means validated and enqueued. Calls on different streams may run concurrently as
+ *    long as they do not share an output or a workspace.
+ *  - Errors: arguments are checked on the host before anything is enqueued; no exception ever
+ *    crosses this boundary. Kernels never trap: a device-side wait that runs past its time limit
+ *    sets the device status word, which fa_get_device_status reports.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, Hq % Hkv != 0, bad lengths */
+  FA_ERR_UNSUPPORTED = 2,     /* head dim not 64/128, page size not in {16,32,64,128}, too large */
+  FA_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = 4,       /* workspace missing or smaller than fa_paged_workspace_bytes() */
+  FA_ERR_CUDA = 5,            /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_NO_DEVICE = 6,       /* current device is not an sm_103 GPU */
+  FA_ERR_DEVICE_TIMEOUT = 7,  /* a kernel gave up waiting on a pipeline barrier (device status) */
+  FA_ERR_DEVICE_BAD_PAGE = 8  /* a kernel met a page id outside [0, num_pages) (device status) */
+} fa_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Dense attention forward ("FlashAttention: tiling + online softmax").
+ *   q, o: [B, S, Hq, d] bf16;  k, v: [B, S, Hkv, d] bf16;  lse: [B, S, Hq] fp32 or NULL (skip).
+ *   scale multiplies q.k before the softmax (usually 1/sqrt(d)).
+ * Returns FA_OK when enqueued. B, S, Hq, Hkv >= 1.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int S, int d, int causal, float scale, fa_stream_t stream);
+
+/*
+ * Paged, ragged attention forward ("FlashInfer: I/O-aware attention for serving").
+ *   q, o:          [total_q, Hq, d] bf16, sequences packed back to back;
+ *   k_pages, v_pages: [num_pages, page_size, Hkv, d] bf16 (a shared page pool);
+ *   page_table:    [num_seqs, max_pages_per_seq] int32 physical page ids; entries past a
+ *                  sequence's last page are never read (may be -1);
+ *   cu_seqlens_q:  [num_seqs + 1] int32 prefix sums of query lengths (cu[0] = 0,
+ *                  cu[num_seqs] = total_q);
+ *   kv_lens:       [num_seqs] int32 key/value lengths, 0 <= kv_len <= max_pages_per_seq*page_size;
+ *   lse:           [total_q, Hq] fp32 or NULL.
+ *   max_q_len:     the largest query length (a host-side bound, used for planning). When it is 1
+ *                  the batch is decoded with split-KV (each sequence's keys are split into
+ *                  num_splits chunks, attended in parallel, and merged by their LSE);
+ *                  otherwise the tiled tensor-core prefill kernel runs.
+ *   num_splits:    split count for decode; 0 chooses one from the SM count.
+ *   workspace:     device scratch of at least fa_paged_workspace_bytes(...) bytes (may be NULL
+ *                  when that function returns 0). Its contents need no initialisation; calls that
+ *                  share a workspace must be ordered on one stream.
+ * Device arrays (page_table, cu_seqlens_q, kv_lens) are read on the device only.
+ */
+fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages,
+                       const int32_t* page_table, const int32_t* cu_seqlens_q,
+                       const int32_t* kv_lens, int num_seqs, int total_q, int max_q_len,
+                       int page_size, int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d,
+                       int causal, float scale, void* o, float* lse, void* workspace,
+                       size_t workspace_bytes, int num_splits, fa_stream_t stream);
+
+/* Workspace bytes fa_paged_fwd needs for these sizes (same num_splits argument, 0 = auto). */
+size_t fa_paged_workspace_bytes(int num_seqs, int total_q, int max_q_len, int page_size,
+                                int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d,
+                                int num_splits);
+
+/* The split count fa_paged_fwd uses for a decode batch with these sizes (num_splits = 0). */
+int fa_decode_num_splits(int num_seqs, int page_size, int max_pages_per_seq, int num_pages,
+                         int Hkv);
+
+/*
+ * Merge partial attention states (the LSE-weighted combine of split-KV decode).
+ *   o_parts:   [num_parts, n_rows, H, d] fp32, each part normalised over its own keys;
+ *   lse_parts: [num_parts, n_rows, H] fp32 (natural log; -inf marks a part with no keys);
+ *   o:         [n_rows, H, d] bf16;  lse: [n_rows, H] fp32 or NULL.
+ * Result: lse = ln sum_p exp(lse_p);  O = sum_p exp(lse_p - lse) * O_p  (O = 0 if all parts
+ * are empty). Equivalent to attending over the union of the parts' keys.
+ */
+fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_parts, int n_rows,
+                          int H, int d, void* o, float* lse, fa_stream_t stream);
+
+/*
+ * Read and clear this GPU's device status word. Synchronises `stream` first.
+ * *code receives FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BAD_PAGE; *site (may be NULL) a
+ * small id of the place in the kernels that recorded it. Returns FA_ERR_CUDA if the synchronisation itself failed.
+ */
+fa_status fa_get_device_status(fa_stream_t stream, int* code, int* site);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

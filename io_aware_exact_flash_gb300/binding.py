@@ -1,0 +1,193 @@
+"""Thin Python binding over the C ABI in ``include/fa.h`` (library ``libfa_gb300.so``).
+
+Every function here only marshals arguments: it checks tensor dtypes, devices and shapes,
+allocates outputs with torch when the caller passes none, and forwards raw device pointers and
+the current CUDA stream to the C entry point of the same name. All attention arithmetic runs in
+the library's sm_103a kernels; there is no other path. If the library is missing, loading fails
+with an error that says so.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .buildlib import LIBRARY
+
+FA_OK = 0
+_STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
+    4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_NO_DEVICE", 7: "FA_ERR_DEVICE_TIMEOUT",
+    8: "FA_ERR_DEVICE_BAD_PAGE",
+}
+
+EXPORTED = ("fa_status_string", "fa_fwd", "fa_paged_fwd", "fa_paged_workspace_bytes",
+            "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status")
+
+
+class FaError(RuntimeError):
+    """A non-OK status returned by the library."""
+
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} returned {_STATUS_NAMES.get(code, code)}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIBRARY) -> ctypes.CDLL:
+    """Load (once) the compiled library and declare its C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA extension not built: {path} is missing (run __graft_entry__.build() or "
+            "python -m io_aware_exact_flash_gb300.buildlib)")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, i, f, vp, vp, vp, sz, i, vp]
+    lib.fa_paged_fwd.restype = i
+    lib.fa_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i, i]
+    lib.fa_paged_workspace_bytes.restype = sz
+    lib.fa_decode_num_splits.argtypes = [i, i, i, i, i]
+    lib.fa_decode_num_splits.restype = i
+    lib.fa_merge_states.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
+    lib.fa_merge_states.restype = i
+    lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i), ctypes.POINTER(i)]
+    lib.fa_get_device_status.restype = i
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, code: int):
+    if code != FA_OK:
+        raise FaError(fn, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bf16_cuda(name, t, dim):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if t.dim() != dim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dim}-D tensor")
+
+
+def _i32_cuda(name, t):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+
+
+def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """Dense attention forward. q: [B, S, Hq, d]; k, v: [B, S, Hkv, d] (bf16, CUDA).
+
+    Returns (o [B, S, Hq, d] bf16, lse [B, S, Hq] fp32 or None)."""
+    _bf16_cuda("q", q, 4)
+    _bf16_cuda("k", k, 4)
+    _bf16_cuda("v", v, 4)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, S, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, S, Hkv, d] matching q")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, S, Hq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    code = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, d, int(bool(causal)), scale,
+                      _stream(stream))
+    _check("fa_fwd", code)
+    return out, lse
+
+
+def fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d,
+                             num_splits=0):
+    return int(load_library().fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq,
+                                                       num_pages, Hq, Hkv, d, num_splits))
+
+
+def fa_decode_num_splits(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv):
+    return int(load_library().fa_decode_num_splits(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv))
+
+
+def fa_paged_fwd(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, max_q_len, causal=True, scale=None,
+                 out=None, lse=None, return_lse=True, workspace=None, num_splits=0, stream=None):
+    """Paged, ragged attention forward.
+
+    q: [total_q, Hq, d]; k_pages, v_pages: [num_pages, page_size, Hkv, d] (bf16, CUDA);
+    page_table: [num_seqs, max_pages_per_seq], cu_seqlens_q: [num_seqs + 1], kv_lens: [num_seqs]
+    (int32, CUDA). max_q_len is a host-side int. Returns (o, lse)."""
+    _bf16_cuda("q", q, 3)
+    _bf16_cuda("k_pages", k_pages, 4)
+    _bf16_cuda("v_pages", v_pages, 4)
+    for name, t in (("page_table", page_table), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens)):
+        _i32_cuda(name, t)
+    total_q, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_pages.shape
+    num_seqs, max_pages = page_table.shape
+    if dk != d or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    need = fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages, num_pages, Hq, Hkv, d,
+                                    num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = load_library()
+    code = lib.fa_paged_fwd(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(cu_seqlens_q),
+                            _ptr(kv_lens), num_seqs, total_q, int(max_q_len), page_size, max_pages, num_pages, Hq,
+                            Hkv, d, int(bool(causal)), scale, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                            int(num_splits), _stream(stream))
+    _check("fa_paged_fwd", code)
+    return out, lse
+
+
+def fa_merge_states(o_parts, lse_parts, out=None, lse=None, return_lse=True, stream=None):
+    """Merge partial states: o_parts [P, n, H, d] fp32, lse_parts [P, n, H] fp32 (natural log)."""
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32 or not o_parts.is_cuda:
+        raise TypeError("o_parts and lse_parts must be CUDA float32 tensors")
+    if not (o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("o_parts and lse_parts must be contiguous")
+    P, n, H, d = o_parts.shape
+    if lse_parts.shape != (P, n, H):
+        raise ValueError("lse_parts must be [P, n, H]")
+    if out is None:
+        out = torch.empty((n, H, d), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None and return_lse:
+        lse = torch.empty((n, H), dtype=torch.float32, device=o_parts.device)
+    code = load_library().fa_merge_states(_ptr(o_parts), _ptr(lse_parts), P, n, H, d, _ptr(out), _ptr(lse),
+                                          _stream(stream))
+    _check("fa_merge_states", code)
+    return out, lse
+
+
+def fa_get_device_status(stream=None):
+    """Returns (code, site) of this GPU's device status word and clears it (synchronises)."""
+    code, site = ctypes.c_int(0), ctypes.c_int(0)
+    _check("fa_get_device_status",
+           load_library().fa_get_device_status(_stream(stream), ctypes.byref(code), ctypes.byref(site)))
+    return code.value, site.value
+
+
+def status_string(code: int) -> str:
+    return load_library().fa_status_string(code).decode()

@@ -1,0 +1,376 @@
+// C ABI of the attention library (declared in include/fa.h): argument validation, TMA tensor
+// descriptors, work planning and kernel dispatch. Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include "../../include/fa.h"
+#include "kernels.cuh"
+
+// The one piece of global device state: a status word per GPU that kernels set instead of
+// trapping (a wait that timed out, a page id outside the pool).
+__device__ fa::DeviceStatus g_fa_device_status;
+
+namespace {
+
+using fa::DeviceStatus;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int sm_count = 0;
+  DeviceStatus* status = nullptr;  // device address of g_fa_device_status on this GPU
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Looks up (once per GPU) whether the current device is an sm_103 part, its SM count and the
+// device address of the status word. Returns nullptr on failure.
+const DeviceInfo* current_device(fa_status* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = FA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& info = g_dev[dev];
+  if (!info.probed) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      *err = FA_ERR_CUDA;
+      return nullptr;
+    }
+    info.supported = (prop.major == 10 && prop.minor == 3);
+    info.sm_count = prop.multiProcessorCount;
+    void* addr = nullptr;
+    if (info.supported) {
+      if (cudaGetSymbolAddress(&addr, g_fa_device_status) != cudaSuccess) {
+        *err = FA_ERR_CUDA;
+        return nullptr;
+      }
+    }
+    info.status = static_cast<DeviceStatus*>(addr);
+    info.probed = true;
+  }
+  if (!info.supported) {
+    *err = FA_ERR_NO_DEVICE;
+    return nullptr;
+  }
+  return &info;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once (no link-time dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 4-D bf16 tensor map with 128-byte swizzle; dims innermost first, strides in bytes for dims 1..3.
+bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides[3],
+              const uint32_t box[4]) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t bd[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, bd, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- paged planning helpers
+struct DecodePlan {
+  int splits;
+  int pages_per_split;
+  int heads_per_cta;
+};
+
+int blocks_of_pages(int pages, int page_size) { return pages * (page_size / 16); }
+
+DecodePlan plan_decode(int num_seqs, int page_size, int max_pages_per_seq, int num_pages, int Hkv, int num_splits,
+                       int sm_count) {
+  DecodePlan d;
+  d.heads_per_cta = Hkv <= 8 ? Hkv : 8;
+  while (Hkv % d.heads_per_cta) --d.heads_per_cta;
+  const int head_blocks = Hkv / d.heads_per_cta;
+  int splits = num_splits;
+  if (splits <= 0) {
+    // Aim for about eight CTAs per SM over the whole batch: the pool holds about num_pages pages
+    // in use, and the longest sequence sets how many splits are needed to cut it that finely.
+    const long long target_ctas = 8LL * (sm_count > 0 ? sm_count : 148);
+    const long long work_pages = (long long)(num_pages > 0 ? num_pages : num_seqs) * head_blocks;
+    long long pps = (work_pages + target_ctas - 1) / target_ctas;
+    if (pps < 1) pps = 1;
+    splits = (int)((max_pages_per_seq + pps - 1) / pps);
+    if (splits < 1) splits = 1;
+    if (splits > 256) splits = 256;
+  }
+  if (splits > max_pages_per_seq) splits = max_pages_per_seq > 0 ? max_pages_per_seq : 1;
+  d.splits = splits;
+  d.pages_per_split = (max_pages_per_seq + splits - 1) / splits;
+  if (d.pages_per_split < 1) d.pages_per_split = 1;
+  return d;
+}
+
+int prefill_max_items(int num_seqs, int total_q) { return total_q / 256 + num_seqs; }
+
+size_t decode_workspace(int num_seqs, int Hq, int d, int splits) {
+  if (splits <= 1) return 0;
+  const size_t o_bytes = align_up((size_t)splits * num_seqs * Hq * d * sizeof(float), 256);
+  const size_t l_bytes = align_up((size_t)splits * num_seqs * Hq * sizeof(float), 256);
+  return o_bytes + l_bytes;
+}
+
+size_t prefill_workspace(int num_seqs, int total_q) {
+  return 256 + align_up((size_t)prefill_max_items(num_seqs, total_q) * sizeof(int2), 256);
+}
+
+int sm_count_now() {
+  fa_status e;
+  const DeviceInfo* info = current_device(&e);
+  if (info) return info->sm_count;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    return n;
+  return 148;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_NO_DEVICE: return "FA_ERR_NO_DEVICE";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    case FA_ERR_DEVICE_BAD_PAGE: return "FA_ERR_DEVICE_BAD_PAGE";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
+                 int d, int causal, float scale, fa_stream_t stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Hq % Hkv != 0 || !scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * S > (1LL << 31) - 1 || (long long)B * S * Hq * d > (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FA_ERR_ALIGNMENT;
+  fa_status err = FA_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+
+  fa::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  const uint32_t box[4] = {64, 1, (uint32_t)fa::kBM, 1};
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)S, (uint64_t)B};
+    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)S * Hq * d * 2};
+    if (!make_map(&p.tm_q, q, dims, str, box)) return FA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)S, (uint64_t)B};
+    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2, (uint64_t)S * Hkv * d * 2};
+    if (!make_map(&p.tm_k, k, dims, str, box) || !make_map(&p.tm_v, v, dims, str, box)) return FA_ERR_CUDA;
+  }
+  p.o = o;
+  p.lse = lse;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.B = B;
+  p.S = S;
+  p.status = dev->status;
+  return fa::launch_prefill_dense(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_decode_num_splits(int num_seqs, int page_size, int max_pages_per_seq, int num_pages, int Hkv) {
+  if (num_seqs <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || Hkv <= 0) return 1;
+  return plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, 0, sm_count_now()).splits;
+}
+
+size_t fa_paged_workspace_bytes(int num_seqs, int total_q, int max_q_len, int page_size, int max_pages_per_seq,
+                                int num_pages, int Hq, int Hkv, int d, int num_splits) {
+  if (num_seqs <= 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0)
+    return 0;
+  if (max_q_len == 1) {
+    const DecodePlan dp =
+        plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, sm_count_now());
+    return decode_workspace(num_seqs, Hq, d, dp.splits);
+  }
+  return prefill_workspace(num_seqs, total_q);
+}
+
+fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                       const int32_t* cu_seqlens_q, const int32_t* kv_lens, int num_seqs, int total_q, int max_q_len,
+                       int page_size, int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d, int causal,
+                       float scale, void* o, float* lse, void* workspace, size_t workspace_bytes, int num_splits,
+                       fa_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !page_table || !cu_seqlens_q || !kv_lens || !o) return FA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || total_q < 0 || max_q_len < 1 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0 ||
+      Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0 || !scale_ok(scale))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)max_pages_per_seq * page_size > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31) - 1)
+    return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+    return FA_ERR_ALIGNMENT;
+  fa_status err = FA_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+  if (total_q == 0) return FA_OK;
+  const int group = Hq / Hkv;
+
+  if (max_q_len == 1) {
+    // ------------------------------------------------------------- split-KV decode
+    if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
+    const DecodePlan dp =
+        plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, dev->sm_count);
+    const size_t need = decode_workspace(num_seqs, Hq, d, dp.splits);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_ALIGNMENT;
+    fa::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.k_pages = k_pages;
+    p.v_pages = v_pages;
+    p.page_table = page_table;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.kv_lens = kv_lens;
+    p.o = o;
+    p.lse = lse;
+    if (need > 0) {
+      p.o_part = static_cast<float*>(workspace);
+      p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            align_up((size_t)dp.splits * num_seqs * Hq * d * sizeof(float), 256));
+    }
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = group;
+    p.page_size = page_size;
+    p.max_pages_per_seq = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.pages_per_split = dp.pages_per_split;
+    p.num_splits = dp.splits;
+    p.heads_per_cta = dp.heads_per_cta;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.status = dev->status;
+    return fa::launch_decode(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  // --------------------------------------------------------------- tensor-core prefill
+  const size_t need = prefill_workspace(num_seqs, total_q);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+  fa::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
+    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)fa::kBM, 1};
+    if (!make_map(&p.tm_q, q, dims, str, box)) return FA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)num_pages};
+    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2, (uint64_t)page_size * Hkv * d * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)page_size, 1};
+    if (!make_map(&p.tm_k, k_pages, dims, str, box) || !make_map(&p.tm_v, v_pages, dims, str, box))
+      return FA_ERR_CUDA;
+  }
+  int* work_count = static_cast<int*>(workspace);
+  int2* work_list = reinterpret_cast<int2*>(static_cast<char*>(workspace) + 256);
+  p.o = o;
+  p.lse = lse;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = group;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.page_table = page_table;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.kv_lens = kv_lens;
+  p.page_size = page_size;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.work_list = work_list;
+  p.work_count = work_count;
+  p.status = dev->status;
+  long long max_kv_tiles = ((long long)max_pages_per_seq * page_size + fa::kBN - 1) / fa::kBN;
+  if (max_kv_tiles > 8192) max_kv_tiles = 8192;  // cost buckets only order the work
+  return fa::launch_prefill_paged(p, d, prefill_max_items(num_seqs, total_q), (int)max_kv_tiles, work_list, work_count,
+                                  stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_parts, int n_rows, int H, int d,
+                          void* o, float* lse, fa_stream_t stream) {
+  if (!o_parts || !lse_parts || !o) return FA_ERR_INVALID_ARG;
+  if (num_parts <= 0 || n_rows <= 0 || H <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FA_ERR_ALIGNMENT;
+  fa_status err = FA_OK;
+  if (!current_device(&err)) return err;
+  return fa::launch_merge(o_parts, lse_parts, num_parts, n_rows, H, d, o, lse, false, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_get_device_status(fa_stream_t stream, int* code, int* site) {
+  if (!code) return FA_ERR_INVALID_ARG;
+  fa_status err = FA_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceStatus h{0, 0};
+  if (cudaMemcpy(&h, dev->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const DeviceStatus zero{0, 0};
+  if (cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  *code = (int)h.code;
+  if (site) *site = (int)h.where;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Shared declarations between the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "ptx.cuh"
+
+namespace fa {
+
+// Tile shape of the tensor-core prefill kernel: each CTA owns two 128-row query tiles (one per
+// softmax warpgroup) and streams 128-row key/value tiles.
+constexpr int kBM = 128;   // query rows per tile (one TMEM lane per row)
+constexpr int kBN = 128;   // keys per tile
+constexpr int kQTiles = 2; // query tiles per CTA (ping-pong between the two softmax warpgroups)
+constexpr int kPrefillThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 spare, 4-11 softmax
+
+struct alignas(64) PrefillParams {
+  CUtensorMap tm_q;  // dense: (d, Hq, S, B)        paged: (d, Hq, total_q, 1)
+  CUtensorMap tm_k;  // dense: (d, Hkv, S, B)       paged: (d, Hkv, page_size, num_pages)
+  CUtensorMap tm_v;
+  void* o;           // bf16 output
+  float* lse;        // fp32 output or null
+  int Hq, Hkv, group;
+  int causal;
+  float scale_log2;  // scale * log2(e)
+  // dense
+  int B, S;
+  // paged
+  const int32_t* page_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* kv_lens;
+  int page_size, max_pages_per_seq, num_pages, num_seqs;
+  int64_t total_q;         // rows of q/o/lse; no row at or past it is ever written
+  const int2* work_list;   // (sequence, query-tile pair) items, heaviest first
+  const int* work_count;
+  DeviceStatus* status;
+};
+
+struct DecodeParams {
+  const void* q;           // [total_q = num_seqs, Hq, d] bf16
+  const void* k_pages;     // [num_pages, page_size, Hkv, d]
+  const void* v_pages;
+  const int32_t* page_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* kv_lens;
+  void* o;                 // bf16 [total_q, Hq, d] (used when num_splits == 1)
+  float* lse;              // fp32 [total_q, Hq] or null
+  float* o_part;           // fp32 [num_splits, num_seqs, Hq, d]
+  float* lse_part;         // fp32 [num_splits, num_seqs, Hq]  (log2 domain, scaled)
+  int num_seqs, Hq, Hkv, group, page_size, max_pages_per_seq, num_pages;
+  int64_t total_q;
+  int pages_per_split, num_splits;
+  int heads_per_cta;       // kv heads one CTA handles
+  float scale_log2;
+  DeviceStatus* status;
+};
+
+// Launchers (return cudaGetLastError() of the launch)
+cudaError_t launch_prefill_dense(const PrefillParams& p, int d, cudaStream_t stream);
+cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int max_items, int max_kv_tiles,
+                                 int2* work_list, int* work_count, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H,
+                         int d, void* o, float* lse, bool log2_domain, cudaStream_t stream);
+
+}  // namespace fa

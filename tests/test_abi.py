@@ -1,0 +1,112 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function include/fa.h
+declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from io_aware_exact_flash_gb300 import buildlib
+
+    if not os.path.exists(buildlib.LIBRARY):
+        if shutil.which(buildlib.NVCC) is None and not os.path.exists(buildlib.NVCC):
+            pytest.skip("nvcc not available to build the library")
+        buildlib.build()
+    from io_aware_exact_flash_gb300 import binding
+
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_paged_fwd", "fa_paged_workspace_bytes", "fa_merge_states", "fa_get_device_status",
+              "fa_status_string", "fa_decode_num_splits"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from io_aware_exact_flash_gb300 import binding
+
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in fa.h but not exported"
+    assert set(binding.EXPORTED) == set(names)
+
+
+def test_status_strings(lib):
+    from io_aware_exact_flash_gb300 import binding
+
+    for code, name in binding._STATUS_NAMES.items():
+        assert binding.status_string(code) == name
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced: validation fails first
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=2, S=128, d=128, causal=1, scale=0.1):
+    vp = ctypes.c_void_p
+    return lib.fa_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse) if lse else None, B, Hq, Hkv, S, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(o=0), 1), (dict(B=0), 1), (dict(S=-1), 1), (dict(Hq=3, Hkv=2), 1),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
+    (dict(d=96), 2), (dict(d=256), 2),
+    (dict(q=FAKE + 8), 3), (dict(v=FAKE + 2), 3), (dict(lse=FAKE + 2), 3),
+])
+def test_fa_fwd_host_validation(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _paged(lib, **kw):
+    a = dict(q=FAKE, kp=FAKE, vp_=FAKE, pt=FAKE, cu=FAKE, kl=FAKE, num_seqs=2, total_q=10, max_q_len=5, ps=16,
+             max_pages=4, num_pages=8, Hq=4, Hkv=2, d=128, causal=1, scale=0.1, o=FAKE, lse=None, ws=None, wsb=0,
+             splits=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.fa_paged_fwd(vp(a["q"]), vp(a["kp"]), vp(a["vp_"]), vp(a["pt"]), vp(a["cu"]), vp(a["kl"]),
+                            a["num_seqs"], a["total_q"], a["max_q_len"], a["ps"], a["max_pages"], a["num_pages"],
+                            a["Hq"], a["Hkv"], a["d"], a["causal"], a["scale"], vp(a["o"]),
+                            vp(a["lse"]) if a["lse"] else None, vp(a["ws"]) if a["ws"] else None, a["wsb"],
+                            a["splits"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(pt=0), 1), (dict(cu=0), 1), (dict(num_seqs=0), 1), (dict(max_q_len=0), 1), (dict(Hq=3), 1),
+    (dict(num_pages=0), 1), (dict(splits=-1), 1),
+    (dict(ps=8), 2), (dict(ps=48), 2), (dict(d=80), 2),
+    (dict(kp=FAKE + 4), 3), (dict(cu=FAKE + 2), 3),
+])
+def test_fa_paged_fwd_host_validation(lib, kw, code):
+    assert _paged(lib, **kw) == code
+
+
+def test_workspace_query_is_host_only(lib):
+    from io_aware_exact_flash_gb300 import binding
+
+    n_prefill = binding.fa_paged_workspace_bytes(64, 300000, 8192, 16, 512, 20000, 32, 8, 128)
+    assert n_prefill >= 8 * (300000 // 256 + 64)
+    assert binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 32, 8, 128, num_splits=1) == 0
+    n4 = binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 32, 8, 128, num_splits=4)
+    assert n4 >= 4 * 64 * 32 * (128 + 1) * 4
+
+
+def test_merge_host_validation(lib):
+    vp = ctypes.c_void_p
+    assert lib.fa_merge_states(None, vp(FAKE), 2, 4, 8, 128, vp(FAKE), None, None) == 1
+    assert lib.fa_merge_states(vp(FAKE), vp(FAKE), 0, 4, 8, 128, vp(FAKE), None, None) == 1
+    assert lib.fa_merge_states(vp(FAKE), vp(FAKE), 2, 4, 8, 100, vp(FAKE), None, None) == 2
+    assert lib.fa_merge_states(vp(FAKE + 4), vp(FAKE), 2, 4, 8, 128, vp(FAKE), None, None) == 3

@@ -1,0 +1,155 @@
+"""Dense attention forward on the GPU against the fp64 oracle, element by element (small and
+ragged shapes) and on sampled rows of the full-size long-context workloads."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_flash_gb300.workloads import WORKLOADS, make_dense, normal_bf16
+from tests.helpers import bf16_to_f64, compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fa(q, k, v, causal, scale):
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    o, lse = fa.fa_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+
+
+CASES = [
+    # (B, S, Hq, Hkv, d, causal)
+    (1, 256, 2, 2, 64, False),    # the small non-causal workload
+    (1, 256, 2, 2, 64, True),
+    (1, 128, 1, 1, 128, False),   # one query tile: the CTA's second tile is empty
+    (1, 128, 1, 1, 128, True),
+    (2, 384, 4, 4, 128, True),    # a CTA with two tiles and one with one
+    (1, 1, 1, 1, 64, True),       # S = 1
+    (1, 1, 1, 1, 128, False),
+    (1, 200, 2, 1, 128, True),    # ragged tail, GQA 2
+    (2, 517, 8, 2, 128, True),    # several tiles + ragged tail, GQA 4
+    (1, 1000, 2, 2, 64, False),
+    (1, 777, 4, 1, 64, True),
+    (3, 640, 2, 2, 128, False),
+    (1, 2048, 2, 2, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,d,causal", CASES)
+def test_dense_matches_oracle(B, S, Hq, Hkv, d, causal):
+    seed = 7 + S + 31 * Hq + d
+    q = normal_bf16(seed, (B, S, Hq, d), stream=0)
+    k = normal_bf16(seed, (B, S, Hkv, d), stream=1)
+    v = normal_bf16(seed, (B, S, Hkv, d), stream=2)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fa(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.get().dense(q, k, v, causal, scale)
+    compare(o, o_ref, lse, lse_ref, f"dense {B, S, Hq, Hkv, d, causal}")
+
+
+@pytest.mark.parametrize("gain", [4.0, 16.0])
+def test_dense_large_scores_force_rescales(gain):
+    """Scores far beyond the deferred-rescale threshold, growing along the sequence, so the
+    running maximum keeps rising and O is rescaled many times."""
+    B, S, H, d = 1, 1024, 2, 128
+    rng = np.random.default_rng(3)
+    from io_aware_exact_flash_gb300.workloads import bf16_bits
+
+    q = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32) * gain)
+    ramp = np.linspace(0.2, 2.0, S, dtype=np.float32)[None, :, None, None]
+    k = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32) * ramp * gain)
+    # V is kept small so |O| < 2 and bf16 output rounding (half an ulp) stays below 4e-3
+    v = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32) * 0.25)
+    for causal in (False, True):
+        o, lse = run_fa(q, k, v, causal, 1.0 / math.sqrt(d))
+        o_ref, lse_ref = oracle.get().dense(q, k, v, causal, 1.0 / math.sqrt(d))
+        compare(o, o_ref, lse, lse_ref, f"large scores gain={gain} causal={causal}")
+
+
+def test_dense_outlier_keys_small():
+    """The long-context recipe (activations x0.5, 1% of key rows x8) at a size the full oracle runs."""
+    from io_aware_exact_flash_gb300.workloads import DenseWorkload
+
+    w = DenseWorkload("outliers_small", B=1, S=1536, Hq=8, Hkv=2, d=128, causal=True, seed=55, act_scale=0.5,
+                      outlier_frac=0.01, outlier_gain=8.0)
+    t = make_dense(w)
+    o, lse = run_fa(t["q"], t["k"], t["v"], True, w.scale)
+    o_ref, lse_ref = oracle.get().dense(t["q"], t["k"], t["v"], True, w.scale)
+    compare(o, o_ref, lse, lse_ref, "outliers")
+
+
+def test_dense_deterministic():
+    q, k, v = (normal_bf16(99, (2, 700, 4, 128), stream=s) for s in range(3))
+    o1, l1 = run_fa(q, k, v, True, 0.09)
+    o2, l2 = run_fa(q, k, v, True, 0.09)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_dense_reads_and_writes_stay_in_bounds():
+    """Inputs sit between NaN guard regions and the output between sentinel regions: a read
+    outside q/k/v would surface as NaN, a write outside o would change a sentinel."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    B, S, H, d = 2, 300, 2, 128
+    n = B * S * H * d
+    guard = 4096
+    tensors = []
+    for s in range(3):
+        bits = normal_bf16(5, (n,), stream=s)
+        buf = torch.full((n + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        buf[guard:guard + n] = to_dev(bits)
+        tensors.append((bits.reshape(B, S, H, d), buf[guard:guard + n].view(B, S, H, d)))
+    obuf = torch.full((n + 2 * guard,), 3.0, dtype=torch.bfloat16, device="cuda")
+    out = obuf[guard:guard + n].view(B, S, H, d)
+    lbuf = torch.full((B * S * H + 2 * guard,), 7.0, dtype=torch.float32, device="cuda")
+    lse = lbuf[guard:guard + B * S * H].view(B, S, H)
+    fa.fa_fwd(tensors[0][1], tensors[1][1], tensors[2][1], causal=True, scale=0.1, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert bool((obuf[:guard] == 3.0).all()) and bool((obuf[guard + n:] == 3.0).all())
+    assert bool((lbuf[:guard] == 7.0).all()) and bool((lbuf[guard + B * S * H:] == 7.0).all())
+    o_ref, lse_ref = oracle.get().dense(tensors[0][0], tensors[1][0], tensors[2][0], True, 0.1)
+    compare(bf16_to_f64(out), o_ref, lse.cpu().numpy(), lse_ref, "guarded")
+
+
+def _sample_rows(B, S, H, rng, n_random):
+    rows = []
+    fixed = [0, 1, 127, 128, 129, 255, 256, S // 2, S - 129, S - 128, S - 2, S - 1]
+    for b in range(B):
+        for i in fixed:
+            rows.append((b, i, int(rng.integers(H))))
+    for _ in range(n_random):
+        rows.append((int(rng.integers(B)), int(rng.integers(S)), int(rng.integers(H))))
+    return np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name,n_random", [
+    ("causal_prefill_b4_h32_s4096_d128", 400),
+    ("gqa_causal_prefill_b1_hq32_hkv8_s32768_d128", 150),
+])
+def test_full_size_sampled_rows(name, n_random):
+    """The full-size workloads in the launch configuration the benchmark times, checked on
+    sampled rows (tile edges, the first and last rows, and random rows) that the oracle computes
+    one by one."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    w = WORKLOADS[name]
+    t = make_dense(w)
+    o, lse = fa.fa_fwd(to_dev(t["q"]), to_dev(t["k"]), to_dev(t["v"]), causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    rows = _sample_rows(w.B, w.S, w.Hq, np.random.default_rng(0), n_random)
+    o_ref, lse_ref = oracle.get().dense_rows(t["q"], t["k"], t["v"], w.causal, w.scale, rows)
+    ridx = torch.from_numpy(rows).cuda()
+    o_s = o[ridx[:, 0], ridx[:, 1], ridx[:, 2]]
+    l_s = lse[ridx[:, 0], ridx[:, 1], ridx[:, 2]]
+    compare(bf16_to_f64(o_s), o_ref, l_s.cpu().numpy(), lse_ref, name)
+    # properties that hold at any size: every row finite, LSE finite
+    assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())

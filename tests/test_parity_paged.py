@@ -1,0 +1,164 @@
+"""Paged, ragged attention (prefill through the tensor-core kernel, decode through split-KV)
+on the GPU against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_flash_gb300.workloads import WORKLOADS, PagedWorkload, make_paged
+from tests.helpers import bf16_to_f64, compare, i32_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+NAN_BF16 = np.uint16(0x7FC0)
+
+
+def build_case(lengths, Hq, Hkv, d, page_size, decode, seed, q_lens=None, extra_pages=0, poison=True):
+    """Paged inputs for the given kv lengths (q_len = kv_len for prefill, 1 for decode, or
+    explicit q_lens). Unused slots of last pages and `extra_pages` unreferenced pool pages hold
+    NaN when poison is set, so any read of them would show in the output."""
+    w = PagedWorkload("case", num_seqs=len(lengths), len_lo=0, len_hi=0, Hq=Hq, Hkv=Hkv, d=d,
+                      page_size=page_size, causal=True, decode=decode, seed=seed, lengths=list(lengths))
+    t = make_paged(w)
+    if q_lens is not None:
+        from io_aware_exact_flash_gb300.workloads import normal_bf16
+
+        q_lens = np.asarray(q_lens, np.int32)
+        cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+        t["cu_seqlens_q"] = cu
+        t["q_lens"] = q_lens
+        t["q"] = normal_bf16(seed + 1, (int(cu[-1]), Hq, d), stream=20)
+        t["total_q"] = int(cu[-1])
+    kp, vp = t["k_pages"], t["v_pages"]
+    if extra_pages:
+        shape = (extra_pages,) + kp.shape[1:]
+        kp = np.concatenate([kp, np.full(shape, NAN_BF16)])
+        vp = np.concatenate([vp, np.full(shape, NAN_BF16)])
+    if poison:
+        kp, vp = kp.copy(), vp.copy()
+        for s, L in enumerate(t["kv_lens"].tolist()):
+            if L % page_size:
+                last = t["page_table"][s, (L - 1) // page_size]
+                kp[last, L % page_size:] = NAN_BF16
+                vp[last, L % page_size:] = NAN_BF16
+    t["k_pages"], t["v_pages"] = kp, vp
+    t["num_pages"] = kp.shape[0]
+    return t
+
+
+def run_paged(t, causal, scale, num_splits=0):
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    max_q = int(t["q_lens"].max()) if len(t["q_lens"]) else 1
+    o, lse = fa.fa_paged_fwd(to_dev(t["q"]), to_dev(t["k_pages"]), to_dev(t["v_pages"]), i32_dev(t["page_table"]),
+                             i32_dev(t["cu_seqlens_q"]), i32_dev(t["kv_lens"]), max_q_len=max(1, max_q),
+                             causal=causal, scale=scale, num_splits=num_splits)
+    torch.cuda.synchronize()
+    code, site = fa.fa_get_device_status()
+    assert code == 0, f"device status {code} at site {site}"
+    return bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+
+
+def oracle_paged(t, causal, scale):
+    return oracle.get().paged(t["q"], t["k_pages"], t["v_pages"], t["page_table"], t["cu_seqlens_q"], t["kv_lens"],
+                              causal, scale)
+
+
+PREFILL_LENGTHS = [1, 15, 16, 17, 100, 128, 129, 255, 256, 257, 300, 513]
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+def test_paged_prefill_page_sizes(page_size):
+    t = build_case(PREFILL_LENGTHS, 8, 2, 128, page_size, False, 11 + page_size, extra_pages=3)
+    scale = 1 / math.sqrt(128)
+    o, lse = run_paged(t, True, scale)
+    o_ref, lse_ref = oracle_paged(t, True, scale)
+    compare(o, o_ref, lse, lse_ref, f"paged prefill ps={page_size}")
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,causal", [(64, 4, 4, True), (128, 4, 1, False), (64, 8, 1, False),
+                                             (128, 6, 3, True)])
+def test_paged_prefill_heads_and_dims(d, Hq, Hkv, causal):
+    t = build_case([40, 700, 129, 1, 384], Hq, Hkv, d, 16, False, 5 + d + Hq)
+    o, lse = run_paged(t, causal, 1 / math.sqrt(d))
+    o_ref, lse_ref = oracle_paged(t, causal, 1 / math.sqrt(d))
+    compare(o, o_ref, lse, lse_ref, f"paged prefill d={d} Hq={Hq} Hkv={Hkv} causal={causal}")
+
+
+def test_paged_prefill_query_shorter_than_keys():
+    """Chunked prefill: the last q_len tokens of each sequence attend to a longer cached prefix
+    (bottom-right causal alignment)."""
+    lengths = [300, 1000, 77, 512]
+    t = build_case(lengths, 8, 2, 128, 16, False, 21, q_lens=[45, 257, 77, 2])
+    o, lse = run_paged(t, True, 0.08)
+    o_ref, lse_ref = oracle_paged(t, True, 0.08)
+    compare(o, o_ref, lse, lse_ref, "chunked prefill")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 8, 8), (128, 16, 2), (128, 8, 4)])
+def test_paged_decode_splits(splits, d, Hq, Hkv):
+    lengths = [1, 16, 17, 1000, 4096, 3333, 64, 250]
+    t = build_case(lengths, Hq, Hkv, d, 16, True, 31 + d + Hq, extra_pages=2)
+    o, lse = run_paged(t, True, 1 / math.sqrt(d), num_splits=splits)
+    o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(d))
+    compare(o, o_ref, lse, lse_ref, f"decode splits={splits} d={d} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("page_size", [32, 128])
+def test_paged_decode_page_sizes(page_size):
+    t = build_case([5, 130, 999, 2048], 8, 2, 128, page_size, True, 41)
+    o, lse = run_paged(t, True, 0.1, num_splits=3)
+    o_ref, lse_ref = oracle_paged(t, True, 0.1)
+    compare(o, o_ref, lse, lse_ref, f"decode ps={page_size}")
+
+
+def test_paged_decode_empty_sequence():
+    """A sequence with no keys gets O = 0 and LSE = -inf; the others are unaffected."""
+    t = build_case([100, 0, 37], 4, 2, 128, 16, True, 51)
+    for splits in (1, 2):
+        o, lse = run_paged(t, True, 0.1, num_splits=splits)
+        o_ref, lse_ref = oracle_paged(t, True, 0.1)
+        compare(o, o_ref, lse, lse_ref, f"decode with empty sequence, splits={splits}")
+        assert np.all(o[1] == 0) and np.all(np.isneginf(lse[1]))
+
+
+def test_paged_prefill_full_size_sampled():
+    """The ragged paged prefill workload (64 sequences, lengths 512..8192) at full size, in the
+    benchmark's launch configuration, checked on sampled (token, head) rows."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    w = WORKLOADS["paged_prefill_64seq_512_8192_hq32_hkv8_d128_p16"]
+    t = make_paged(w)
+    o, lse = fa.fa_paged_fwd(to_dev(t["q"]), to_dev(t["k_pages"]), to_dev(t["v_pages"]), i32_dev(t["page_table"]),
+                             i32_dev(t["cu_seqlens_q"]), i32_dev(t["kv_lens"]), max_q_len=int(t["q_lens"].max()),
+                             causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    cu = t["cu_seqlens_q"]
+    rows = []
+    for s in range(w.num_seqs):
+        for i in (0, int(t["q_lens"][s]) - 1, int(rng.integers(t["q_lens"][s]))):
+            rows.append((int(cu[s]) + i, int(rng.integers(w.Hq))))
+    rows = np.array(rows, np.int64)
+    o_ref, lse_ref = oracle.get().paged_rows(t["q"], t["k_pages"], t["v_pages"], t["page_table"], cu, t["kv_lens"],
+                                             True, w.scale, rows)
+    ridx = torch.from_numpy(rows).cuda()
+    compare(bf16_to_f64(o[ridx[:, 0], ridx[:, 1]]), o_ref, lse[ridx[:, 0], ridx[:, 1]].cpu().numpy(), lse_ref,
+            "paged prefill full size")
+    assert bool(torch.isfinite(o.float()).all())
+
+
+def test_paged_decode_full_size():
+    """The GQA decode workload (128 sequences, kv lengths 1024..16384) at full size, with the
+    automatic split count the benchmark uses, against the oracle on every row."""
+    w = WORKLOADS["paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16"]
+    t = make_paged(w)
+    o, lse = run_paged(t, True, w.scale, num_splits=0)
+    o_ref, lse_ref = oracle_paged(t, True, w.scale)
+    compare(o, o_ref, lse, lse_ref, "decode full size")
