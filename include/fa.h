@@ -114,6 +114,33 @@ fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_
                           int H, int d, void* o, float* lse, fa_stream_t stream);
 
 /*
+ * Split-KV paged decode for callers that cannot allocate device memory. The pages have no
+ * counterpart of this entry point; it exists for callers that may not call cudaMalloc (for
+ * example an engine whose device memory is all handed to a fixed arena, or a plugin inside a
+ * host that owns every allocation) and so cannot lend fa_paged_fwd a workspace.
+ *   Arguments and results are those of fa_paged_fwd for a decode batch (every query length is
+ *   0 or 1, i.e. max_q_len == 1); inputs and outputs are still the caller's.
+ *   Scratch: the per-split partials live in a fixed device array of FA_NOALLOC_SCRATCH_BYTES
+ *   (16 MiB) inside this library, which every GPU that loads the library holds until the process
+ *   exits. The function itself allocates and frees nothing.
+ *   num_splits > 0 whose partials (num_splits * num_seqs * Hq * (d + 1) * 4 bytes, 256-byte
+ *   aligned per block) exceed the scratch is rejected with FA_ERR_WORKSPACE before anything is
+ *   enqueued; num_splits == 0 lowers the automatic count until the partials fit.
+ *   Sharing: every call on a device uses the same scratch, which keeps the last call's contents
+ *   (nothing in it needs to start at zero). Calls whose kernels overlap on the GPU -- on two
+ *   streams, or from two threads -- race on it; order them on one stream.
+ *   Set-up: the first call on each device looks up the scratch's device address with that device
+ *   current (a host-side symbol lookup). Make that first call before any stream capture.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* page_table, const int32_t* cu_seqlens_q,
+                                  const int32_t* kv_lens, int num_seqs, int total_q, int page_size,
+                                  int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d,
+                                  float scale, void* o, float* lse, int num_splits,
+                                  fa_stream_t stream);
+
+/*
  * Read and clear this GPU's device status word. Synchronises `stream` first.
  * *code receives FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BAD_PAGE; *site (may be NULL) a
  * small id of the place in the kernels that recorded it. Returns FA_ERR_CUDA if the synchronisation itself failed.

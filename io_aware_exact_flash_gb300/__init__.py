@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     fa_fwd,
     fa_get_device_status,
     fa_merge_states,
+    fa_paged_decode_noalloc,
     fa_paged_fwd,
     fa_paged_workspace_bytes,
     load_library,

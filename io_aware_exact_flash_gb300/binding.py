@@ -24,7 +24,7 @@ _STATUS_NAMES = {
 }
 
 EXPORTED = ("fa_status_string", "fa_fwd", "fa_paged_fwd", "fa_paged_workspace_bytes",
-            "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status")
+            "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status", "fa_paged_decode_noalloc")
 
 
 class FaError(RuntimeError):
@@ -61,6 +61,8 @@ def load_library(path: str = LIBRARY) -> ctypes.CDLL:
     lib.fa_decode_num_splits.restype = i
     lib.fa_merge_states.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
     lib.fa_merge_states.restype = i
+    lib.fa_paged_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, i, vp]
+    lib.fa_paged_decode_noalloc.restype = i
     lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i), ctypes.POINTER(i)]
     lib.fa_get_device_status.restype = i
     _lib = lib
@@ -191,3 +193,26 @@ def fa_get_device_status(stream=None):
 
 def status_string(code: int) -> str:
     return load_library().fa_status_string(code).decode()
+
+
+def fa_paged_decode_noalloc(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, out, lse=None, scale=None,
+                            num_splits=0, stream=None):
+    """Split-KV decode that uses the library's fixed device scratch instead of a workspace, for
+    callers that cannot allocate device memory. Nothing is allocated here either: the caller
+    passes `out` ([total_q, Hq, d] bf16) and, optionally, `lse` ([total_q, Hq] fp32)."""
+    _bf16_cuda("q", q, 3)
+    _bf16_cuda("k_pages", k_pages, 4)
+    _bf16_cuda("v_pages", v_pages, 4)
+    _bf16_cuda("out", out, 3)
+    for name, t in (("page_table", page_table), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens)):
+        _i32_cuda(name, t)
+    total_q, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    num_seqs, max_pages = page_table.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code = load_library().fa_paged_decode_noalloc(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens), num_seqs,
+        total_q, page_size, max_pages, num_pages, Hq, Hkv, d, scale, _ptr(out), _ptr(lse), int(num_splits),
+        _stream(stream))
+    _check("fa_paged_decode_noalloc", code)
+    return out, lse

@@ -162,6 +162,15 @@ int sm_count_now() {
 
 }  // namespace
 
+int fa::current_device_info(DeviceStatus** status, int* sm_count) {
+  fa_status err = FA_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+  *status = dev->status;
+  *sm_count = dev->sm_count;
+  return FA_OK;
+}
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {

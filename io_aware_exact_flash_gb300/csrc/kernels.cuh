@@ -55,6 +55,10 @@ struct DecodeParams {
   DeviceStatus* status;
 };
 
+// Status word and SM count of the current device, for entry points defined outside api.cu.
+// Returns 0 (FA_OK) or the fa_status code that describes why the device cannot be used.
+int current_device_info(DeviceStatus** status, int* sm_count);
+
 // Launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_prefill_dense(const PrefillParams& p, int d, cudaStream_t stream);
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int max_items, int max_kv_tiles,
