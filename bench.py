@@ -343,6 +343,28 @@ def run_reference(args, rank, world):
     return 0
 
 
+def profile_only(args, device):
+    """Time one workload by itself (for profiler runs); prints one line with its own metric."""
+    import dataclasses
+
+    import torch
+
+    w = WORKLOADS[args.only]
+    if args.seqs is not None:
+        if not hasattr(w, "num_seqs"):
+            raise SystemExit("--seqs applies to paged workloads")
+        WORKLOADS[args.only] = dataclasses.replace(w, num_seqs=args.seqs)
+    case = (PagedCase if args.only.startswith("paged") else DenseCase)(args.only, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    ms = statistics.mean(time_case(case, args.steps, args.warmup, flush))
+    if case.kind == "decode":
+        out = {"workload": args.only, "seqs": case.w.num_seqs, "ms": ms, "GB/s": case.bytes / (ms * 1e-3) / 1e9}
+    else:
+        out = {"workload": args.only, "ms": ms, "TFLOP/s": case.flops / (ms * 1e-3) / 1e12}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 def main(argv=None):
     ap = argparse.ArgumentParser()
@@ -352,6 +374,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--extras", default="all", help="comma list of extra workloads, 'all' or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="profiling aid: time only this workload (no headline line is printed)")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="profiling aid: override the sequence count of a paged workload given with --only")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -368,6 +394,8 @@ def main(argv=None):
     import io_aware_exact_flash_gb300 as fa
 
     fa.load_library()
+    if args.only is not None:
+        return profile_only(args, device)
     peaks = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 

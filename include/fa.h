@@ -123,12 +123,14 @@ fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_
  *   Scratch: the per-split partials live in a fixed device array of FA_NOALLOC_SCRATCH_BYTES
  *   (16 MiB) inside this library, which every GPU that loads the library holds until the process
  *   exits. The function itself allocates and frees nothing.
- *   num_splits > 0 whose partials (num_splits * num_seqs * Hq * (d + 1) * 4 bytes, 256-byte
- *   aligned per block) exceed the scratch is rejected with FA_ERR_WORKSPACE before anything is
- *   enqueued; num_splits == 0 lowers the automatic count until the partials fit.
- *   Sharing: every call on a device uses the same scratch, which keeps the last call's contents
- *   (nothing in it needs to start at zero). Calls whose kernels overlap on the GPU -- on two
- *   streams, or from two threads -- race on it; order them on one stream.
+ *   num_splits > 0 whose scratch (num_splits * num_seqs * Hq * (d + 1) floats of partials plus
+ *   one int per sequence and block of up to 8 kv heads, each part 256-byte aligned) exceeds the
+ *   array is rejected with FA_ERR_WORKSPACE before anything is enqueued; num_splits == 0 lowers
+ *   the automatic count until it fits.
+ *   Sharing: every call on a device uses the same scratch, which keeps the last call's contents;
+ *   the merge counters in it are cleared by each call (an asynchronous memset on `stream`). Calls
+ *   whose kernels overlap on the GPU -- on two streams, or from two threads -- race on it; order
+ *   them on one stream.
  *   Set-up: the first call on each device looks up the scratch's device address with that device
  *   current (a host-side symbol lookup). Make that first call before any stream capture.
  */

@@ -38,11 +38,14 @@ class FaError(RuntimeError):
 _lib = None
 
 
-def load_library(path: str = LIBRARY) -> ctypes.CDLL:
-    """Load (once) the compiled library and declare its C signatures."""
+def load_library(path: str = None) -> ctypes.CDLL:
+    """Load (once) the compiled library and declare its C signatures. The path defaults to the
+    in-tree build; the environment variable FA_GB300_LIBRARY selects another build of it."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = os.environ.get("FA_GB300_LIBRARY", LIBRARY)
     if not os.path.exists(path):
         raise RuntimeError(
             f"CUDA extension not built: {path} is missing (run __graft_entry__.build() or "

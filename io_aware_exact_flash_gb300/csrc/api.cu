@@ -115,8 +115,7 @@ int blocks_of_pages(int pages, int page_size) { return pages * (page_size / 16);
 DecodePlan plan_decode(int num_seqs, int page_size, int max_pages_per_seq, int num_pages, int Hkv, int num_splits,
                        int sm_count) {
   DecodePlan d;
-  d.heads_per_cta = Hkv <= 8 ? Hkv : 8;
-  while (Hkv % d.heads_per_cta) --d.heads_per_cta;
+  d.heads_per_cta = fa::decode_heads_per_cta(Hkv);
   const int head_blocks = Hkv / d.heads_per_cta;
   int splits = num_splits;
   if (splits <= 0) {
@@ -139,15 +138,13 @@ DecodePlan plan_decode(int num_seqs, int page_size, int max_pages_per_seq, int n
 
 int prefill_max_items(int num_seqs, int total_q) { return total_q / 256 + num_seqs; }
 
-size_t decode_workspace(int num_seqs, int Hq, int d, int splits) {
-  if (splits <= 1) return 0;
-  const size_t o_bytes = align_up((size_t)splits * num_seqs * Hq * d * sizeof(float), 256);
-  const size_t l_bytes = align_up((size_t)splits * num_seqs * Hq * sizeof(float), 256);
-  return o_bytes + l_bytes;
+size_t decode_workspace(int num_seqs, int Hq, int Hkv, int d, int splits) {
+  return fa::decode_scratch_bytes(splits, num_seqs, Hq, Hkv, d);
 }
 
+// count | work list (int2 per item) | sequence order and item offsets (2 ints per sequence)
 size_t prefill_workspace(int num_seqs, int total_q) {
-  return 256 + align_up((size_t)prefill_max_items(num_seqs, total_q) * sizeof(int2), 256);
+  return 256 + align_up((size_t)prefill_max_items(num_seqs, total_q) * sizeof(int2) + 2 * sizeof(int) * num_seqs, 256);
 }
 
 int sm_count_now() {
@@ -222,8 +219,16 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.B = B;
   p.S = S;
+  {
+    // about one wave of CTAs per chunk of kv heads (see the unit order in prefill.cu)
+    const long long per_kv_head = (long long)(Hq / Hkv) * ((S + 255) / 256);
+    long long hc = (dev->sm_count + per_kv_head / 2) / per_kv_head;
+    if (hc < 1) hc = 1;
+    if (hc > (long long)B * Hkv) hc = (long long)B * Hkv;
+    p.kv_heads_per_chunk = (int)hc;
+  }
   p.status = dev->status;
-  return fa::launch_prefill_dense(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return fa::launch_prefill_dense(p, d, dev->sm_count, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_decode_num_splits(int num_seqs, int page_size, int max_pages_per_seq, int num_pages, int Hkv) {
@@ -238,7 +243,7 @@ size_t fa_paged_workspace_bytes(int num_seqs, int total_q, int max_q_len, int pa
   if (max_q_len == 1) {
     const DecodePlan dp =
         plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, sm_count_now());
-    return decode_workspace(num_seqs, Hq, d, dp.splits);
+    return decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);
   }
   return prefill_workspace(num_seqs, total_q);
 }
@@ -271,7 +276,7 @@ fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, 
     if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
     const DecodePlan dp =
         plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, dev->sm_count);
-    const size_t need = decode_workspace(num_seqs, Hq, d, dp.splits);
+    const size_t need = decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);
     if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_ALIGNMENT;
     fa::DecodeParams p;
@@ -284,11 +289,7 @@ fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, 
     p.kv_lens = kv_lens;
     p.o = o;
     p.lse = lse;
-    if (need > 0) {
-      p.o_part = static_cast<float*>(workspace);
-      p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                            align_up((size_t)dp.splits * num_seqs * Hq * d * sizeof(float), 256));
-    }
+    if (need > 0) fa::decode_scratch_layout(workspace, dp.splits, num_seqs, Hq, d, p);
     p.num_seqs = num_seqs;
     p.total_q = total_q;
     p.Hq = Hq;
@@ -346,8 +347,8 @@ fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, 
   p.status = dev->status;
   long long max_kv_tiles = ((long long)max_pages_per_seq * page_size + fa::kBN - 1) / fa::kBN;
   if (max_kv_tiles > 8192) max_kv_tiles = 8192;  // cost buckets only order the work
-  return fa::launch_prefill_paged(p, d, prefill_max_items(num_seqs, total_q), (int)max_kv_tiles, work_list, work_count,
-                                  stream) == cudaSuccess
+  return fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q), (int)max_kv_tiles,
+                                  work_list, work_count, stream) == cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;
 }

@@ -12,8 +12,8 @@
 // copies, one warp per kv head; lane 0 of warp 0 refills a stage as soon as all warps release it. Each warp keeps its group's query heads in registers, computes
 // the scores of 16 rows, updates the running max m and sum l once per block, and accumulates
 // O += p v. A CTA writes one partial state per (split, query head): O normalised over its keys
-// and its LSE. A second kernel merges the splits (or, with one split, the first kernel writes
-// the final O and LSE itself).
+// and its LSE; the last CTA of a sequence to finish merges the splits (with one split the CTA
+// writes the final O and LSE itself).
 #include <cuda_bf16.h>
 #include "kernels.cuh"
 
@@ -223,56 +223,95 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
       for (int e = 0; e < C::EPL; ++e) o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], sh);
     }
   }
-  if (rg != 0) return;
+  if (rg == 0) {
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const int h = hk * G + g;
-    const float inv_l = l[g] > 0.f ? 1.f / l[g] : 0.f;
-    const float lse2 = l[g] > 0.f ? m[g] + __log2f(l[g]) : -INFINITY;
-    if (p.num_splits == 1) {
-      __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((int64_t)tok * p.Hq + h) * D;
-#pragma unroll
-      for (int c = 0; c < C::CPL; ++c) {
-        uint4 w;
-        w.x = pack_bf16x2(o[g][c * 8 + 0] * inv_l, o[g][c * 8 + 1] * inv_l);
-        w.y = pack_bf16x2(o[g][c * 8 + 2] * inv_l, o[g][c * 8 + 3] * inv_l);
-        w.z = pack_bf16x2(o[g][c * 8 + 4] * inv_l, o[g][c * 8 + 5] * inv_l);
-        w.w = pack_bf16x2(o[g][c * 8 + 6] * inv_l, o[g][c * 8 + 7] * inv_l);
-        reinterpret_cast<uint4*>(op)[lr + c * C::LPR] = w;
-      }
-      if (lr == 0 && p.lse) p.lse[(int64_t)tok * p.Hq + h] = lse2 * kLn2;
-    } else {
-      const int64_t prow = ((int64_t)split * p.num_seqs + seq) * p.Hq + h;
-      if (l[g] > 0.f) {
-        float4* op = reinterpret_cast<float4*>(p.o_part + prow * D);
+    for (int g = 0; g < G; ++g) {
+      const int h = hk * G + g;
+      const float inv_l = l[g] > 0.f ? 1.f / l[g] : 0.f;
+      const float lse2 = l[g] > 0.f ? m[g] + __log2f(l[g]) : -INFINITY;
+      if (p.num_splits == 1) {
+        __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((int64_t)tok * p.Hq + h) * D;
 #pragma unroll
         for (int c = 0; c < C::CPL; ++c) {
-          op[2 * (lr + c * C::LPR)] = make_float4(o[g][c * 8 + 0] * inv_l, o[g][c * 8 + 1] * inv_l,
-                                                  o[g][c * 8 + 2] * inv_l, o[g][c * 8 + 3] * inv_l);
-          op[2 * (lr + c * C::LPR) + 1] = make_float4(o[g][c * 8 + 4] * inv_l, o[g][c * 8 + 5] * inv_l,
-                                                      o[g][c * 8 + 6] * inv_l, o[g][c * 8 + 7] * inv_l);
+          uint4 w;
+          w.x = pack_bf16x2(o[g][c * 8 + 0] * inv_l, o[g][c * 8 + 1] * inv_l);
+          w.y = pack_bf16x2(o[g][c * 8 + 2] * inv_l, o[g][c * 8 + 3] * inv_l);
+          w.z = pack_bf16x2(o[g][c * 8 + 4] * inv_l, o[g][c * 8 + 5] * inv_l);
+          w.w = pack_bf16x2(o[g][c * 8 + 6] * inv_l, o[g][c * 8 + 7] * inv_l);
+          reinterpret_cast<uint4*>(op)[lr + c * C::LPR] = w;
         }
+        if (lr == 0 && p.lse) p.lse[(int64_t)tok * p.Hq + h] = lse2 * kLn2;
+      } else {
+        const int64_t prow = ((int64_t)split * p.num_seqs + seq) * p.Hq + h;
+        if (l[g] > 0.f) {
+          float4* op = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+          for (int c = 0; c < C::CPL; ++c) {
+            op[2 * (lr + c * C::LPR)] = make_float4(o[g][c * 8 + 0] * inv_l, o[g][c * 8 + 1] * inv_l,
+                                                    o[g][c * 8 + 2] * inv_l, o[g][c * 8 + 3] * inv_l);
+            op[2 * (lr + c * C::LPR) + 1] = make_float4(o[g][c * 8 + 4] * inv_l, o[g][c * 8 + 5] * inv_l,
+                                                        o[g][c * 8 + 6] * inv_l, o[g][c * 8 + 7] * inv_l);
+          }
+        }
+        if (lr == 0) p.lse_part[prow] = lse2;
       }
-      if (lr == 0) p.lse_part[prow] = lse2;
     }
+  }
+  if (p.num_splits == 1) return;
+
+  // ---------------------------------------------------------------- LSE-weighted merge
+  // The last CTA of this (sequence, kv-head block) to finish merges every split:
+  //   lse = log2 sum_s 2^{lse_s},  O = sum_s 2^{lse_s - lse} O_s
+  // (log2 domain, scaled scores). A split with lse_s = -inf had no keys; its O_s is not read.
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(&p.counters[(int64_t)seq * gridDim.z + blockIdx.z], 1);
+    is_last = (prev == p.num_splits - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  constexpr int kPerHead = D / 4;
+  for (int t = threadIdx.x; t < hpc * G * kPerHead; t += blockDim.x) {
+    const int h = hk0 * G + t / kPerHead, e4 = t % kPerHead;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < p.num_splits; ++sp)
+      mx = fmaxf(mx, __ldcg(&p.lse_part[((int64_t)sp * p.num_seqs + seq) * p.Hq + h]));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int sp = 0; sp < p.num_splits; ++sp) {
+        const int64_t prow = ((int64_t)sp * p.num_seqs + seq) * p.Hq + h;
+        const float ls = __ldcg(&p.lse_part[prow]);
+        if (ls == -INFINITY) continue;
+        const float wgt = ex2(ls - mx);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.o_part + prow * D) + e4);
+        acc.x = fmaf(wgt, v.x, acc.x);
+        acc.y = fmaf(wgt, v.y, acc.y);
+        acc.z = fmaf(wgt, v.z, acc.z);
+        acc.w = fmaf(wgt, v.w, acc.w);
+        wsum += wgt;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.o) + ((int64_t)tok * p.Hq + h) * D)[e4] = packed;
+    if (e4 == 0 && p.lse != nullptr) p.lse[(int64_t)tok * p.Hq + h] = wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
   }
 }
 
 // Merge of partial states, one CTA per row, 4 elements per thread:
 //   lse = log sum_p exp(lse_p),  O = sum_p exp(lse_p - lse) O_p.
 // A part with lse_p = -inf has no keys; its O_p is never read (it may hold any bits).
-// With `cu` set (split-KV decode), part row r is sequence r and its output row is the sequence's
-// query token cu[r]; sequences without a query token are skipped.
 template <bool LOG2>
 __global__ void merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int num_parts,
-                             int n_rows, int H, int D, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                             const int32_t* __restrict__ cu, int64_t total_rows) {
+                             int n_rows, int H, int D, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   const int row = blockIdx.x;
-  int64_t out_row = row;
-  if (cu != nullptr) {
-    out_row = cu[row];
-    if (cu[row + 1] - cu[row] <= 0 || out_row < 0 || out_row >= total_rows) return;
-  }
+  const int64_t out_row = row;
   const int per_head = D / 4;
   for (int t = threadIdx.x; t < H * per_head; t += blockDim.x) {
     const int h = t / per_head, e4 = t % per_head;
@@ -322,12 +361,13 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
     if (dev < 32) configured_smem[dev] = smem;
   }
   dim3 grid(p.num_splits, p.num_seqs, p.Hkv / p.heads_per_cta);
+  if (p.num_splits > 1) {
+    // arrival counters of the fused merge start at zero on every call
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(int) * (size_t)p.num_seqs * (p.Hkv / p.heads_per_cta),
+                                    stream);
+    if (e != cudaSuccess) return e;
+  }
   kern<<<grid, p.heads_per_cta * 32, smem, stream>>>(p, n_stages);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.num_splits == 1) return e;
-  merge_kernel<true><<<p.num_seqs, 256, 0, stream>>>(p.o_part, p.lse_part, p.num_splits, p.num_seqs, p.Hq, D,
-                                                     reinterpret_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_seqlens_q,
-                                                     p.total_q);
   return cudaGetLastError();
 }
 
@@ -356,9 +396,9 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_par
                          float* lse, bool log2_domain, cudaStream_t stream) {
   auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
   if (log2_domain)
-    merge_kernel<true><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, lse, nullptr, n_rows);
+    merge_kernel<true><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, lse);
   else
-    merge_kernel<false><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, lse, nullptr, n_rows);
+    merge_kernel<false><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, lse);
   return cudaGetLastError();
 }
 

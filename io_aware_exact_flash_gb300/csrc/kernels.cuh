@@ -12,7 +12,13 @@ namespace fa {
 constexpr int kBM = 128;   // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;   // keys per tile
 constexpr int kQTiles = 2; // query tiles per CTA (ping-pong between the two softmax warpgroups)
-constexpr int kPrefillThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 spare, 4-11 softmax
+constexpr int kPrefillThreads = 384;  // warp 0 TMA, warps 1-2 MMA, warp 3 spare, 4-11 softmax
+// Registers per thread after the prefill CTA's split: warpgroup 0 (TMA, MMA, spare warps) drops
+// to kRegsControl, the two softmax warpgroups rise to kRegsSoftmax. The sum stays within the
+// 384 x 168 registers the CTA launches with (the launcher checks the compiled count).
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kPrefillThreads * 168, "register split too large");
 
 struct alignas(64) PrefillParams {
   CUtensorMap tm_q;  // dense: (d, Hq, S, B)        paged: (d, Hq, total_q, 1)
@@ -25,6 +31,7 @@ struct alignas(64) PrefillParams {
   float scale_log2;  // scale * log2(e)
   // dense
   int B, S;
+  int kv_heads_per_chunk;  // unit order: kv heads whose query tiles are scheduled together
   // paged
   const int32_t* page_table;
   const int32_t* cu_seqlens_q;
@@ -47,6 +54,7 @@ struct DecodeParams {
   float* lse;              // fp32 [total_q, Hq] or null
   float* o_part;           // fp32 [num_splits, num_seqs, Hq, d]
   float* lse_part;         // fp32 [num_splits, num_seqs, Hq]  (log2 domain, scaled)
+  int* counters;           // [num_seqs, Hkv / heads_per_cta] arrivals of the fused merge
   int num_seqs, Hq, Hkv, group, page_size, max_pages_per_seq, num_pages;
   int64_t total_q;
   int pages_per_split, num_splits;
@@ -55,13 +63,39 @@ struct DecodeParams {
   DeviceStatus* status;
 };
 
+// kv heads one decode CTA handles: the largest divisor of Hkv that is at most 8
+inline int decode_heads_per_cta(int Hkv) {
+  int h = Hkv <= 8 ? Hkv : 8;
+  while (Hkv % h) --h;
+  return h;
+}
+
+// Split-KV decode scratch: partial O | partial LSE | merge counters, each block 256-byte aligned.
+inline size_t decode_scratch_bytes(int splits, int num_seqs, int Hq, int Hkv, int d) {
+  if (splits <= 1) return 0;
+  auto a = [](size_t x) { return (x + 255) / 256 * 256; };
+  return a((size_t)splits * num_seqs * Hq * d * sizeof(float)) + a((size_t)splits * num_seqs * Hq * sizeof(float)) +
+         a((size_t)num_seqs * (Hkv / decode_heads_per_cta(Hkv)) * sizeof(int));
+}
+
+inline void decode_scratch_layout(void* base, int splits, int num_seqs, int Hq, int d, DecodeParams& p) {
+  auto a = [](size_t x) { return (x + 255) / 256 * 256; };
+  char* c = static_cast<char*>(base);
+  p.o_part = reinterpret_cast<float*>(c);
+  c += a((size_t)splits * num_seqs * Hq * d * sizeof(float));
+  p.lse_part = reinterpret_cast<float*>(c);
+  c += a((size_t)splits * num_seqs * Hq * sizeof(float));
+  p.counters = reinterpret_cast<int*>(c);
+}
+
 // Status word and SM count of the current device, for entry points defined outside api.cu.
 // Returns 0 (FA_OK) or the fa_status code that describes why the device cannot be used.
 int current_device_info(DeviceStatus** status, int* sm_count);
 
 // Launchers (return cudaGetLastError() of the launch)
-cudaError_t launch_prefill_dense(const PrefillParams& p, int d, cudaStream_t stream);
-cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int max_items, int max_kv_tiles,
+// Prefill launches are persistent: min(units, sm_count) CTAs loop over the work units.
+cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cudaStream_t stream);
+cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
                                  int2* work_list, int* work_count, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H,

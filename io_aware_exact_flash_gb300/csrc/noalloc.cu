@@ -21,19 +21,15 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoAllocScratchBytes == (size_t)16 << 20, "header and library disagree on the scratch size");
 
-// The shared scratch: partial O values first, then partial LSEs (each block 256-byte aligned).
+// The shared scratch: partial O values, partial LSEs and the merge's arrival counters.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
 
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-size_t partials_bytes(int splits, int num_seqs, int Hq, int d) {
-  if (splits <= 1) return 0;
-  return align256((size_t)splits * num_seqs * Hq * d * sizeof(float)) +
-         align256((size_t)splits * num_seqs * Hq * sizeof(float));
+size_t partials_bytes(int splits, int num_seqs, int Hq, int Hkv, int d) {
+  return fa::decode_scratch_bytes(splits, num_seqs, Hq, Hkv, d);
 }
 
 // Device address of the scratch on the current device. The host-side name of a __device__
@@ -80,10 +76,10 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages,
   // count is lowered until they fit (one split needs no scratch at all).
   int splits = num_splits;
   if (splits > 0) {
-    if (partials_bytes(splits, num_seqs, Hq, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+    if (partials_bytes(splits, num_seqs, Hq, Hkv, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
   } else {
     splits = fa_decode_num_splits(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv);
-    while (splits > 1 && partials_bytes(splits, num_seqs, Hq, d) > kNoAllocScratchBytes) --splits;
+    while (splits > 1 && partials_bytes(splits, num_seqs, Hq, Hkv, d) > kNoAllocScratchBytes) --splits;
   }
   if (splits > max_pages_per_seq) splits = max_pages_per_seq;
   if (splits < 1) splits = 1;
@@ -107,11 +103,7 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages,
   p.kv_lens = kv_lens;
   p.o = o;
   p.lse = lse;
-  if (splits > 1) {
-    p.o_part = static_cast<float*>(scratch);
-    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
-                                          align256((size_t)splits * num_seqs * Hq * d * sizeof(float)));
-  }
+  if (splits > 1) fa::decode_scratch_layout(scratch, splits, num_seqs, Hq, d, p);
   p.num_seqs = num_seqs;
   p.total_q = total_q;
   p.Hq = Hq;
@@ -122,8 +114,7 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages,
   p.num_pages = num_pages;
   p.num_splits = splits;
   p.pages_per_split = (max_pages_per_seq + splits - 1) / splits;
-  p.heads_per_cta = Hkv <= 8 ? Hkv : 8;
-  while (Hkv % p.heads_per_cta) --p.heads_per_cta;
+  p.heads_per_cta = fa::decode_heads_per_cta(Hkv);
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.status = status;
   return fa::launch_decode(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;

@@ -9,16 +9,18 @@
 //
 // CTA organisation (384 threads, one CTA per SM):
 //   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into a ring of stages
-//   warp 1      TMEM owner and MMA issuer (one elected lane issues every tcgen05.mma)
-//   warps 2-3   idle
+//   warp 1      TMEM owner; one lane issues every tcgen05.mma of query tile 0
+//   warp 2      one lane issues every tcgen05.mma of query tile 1
+//   warp 3      idle
 //   warps 4-7   softmax warpgroup 0 -> query tile 0 (rows 0..127 of the CTA's 256)
 //   warps 8-11  softmax warpgroup 1 -> query tile 1 (rows 128..255)
 // The two warpgroups ping-pong: while one computes its softmax the tensor core runs the other's
-// P V and next Q K^T.
+// P V and next Q K^T (the two MMA issuers take turns to keep that order).
 //
 // TMEM columns: S/P of tile g at [128 g, 128 g + 128) (P, as packed bf16 pairs, overwrites the
 // first 64 columns of S), O of tile g at [256 + g D, 256 + (g+1) D).
 #include <cuda_bf16.h>
+#include <cstdlib>
 #include "kernels.cuh"
 
 namespace fa {
@@ -35,7 +37,7 @@ struct Cfg {
   static constexpr int kTileBytes = kBM * D * 2;  // one 128-row tile of Q, K or V (bf16)
   static constexpr int kSub = D / 64;             // 128-byte-wide column blocks per tile
   static constexpr int kSubBytes = kBM * 128;     // 16 KB per column block
-  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kStages = D == 128 ? 5 : 8;
   static constexpr int kSmemBytes = 1024 + (kQTiles + kStages) * kTileBytes;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
@@ -53,7 +55,145 @@ enum : uint32_t {
   kSiteSoftmaxS = 5,
   kSiteSoftmaxO = 6,
   kSiteDrain = 7,
+  kSiteMmaTurn = 8,
 };
+
+// One unit of work: a pair of 128-row query tiles of one (sequence, query head).
+struct Unit {
+  int seq, h, hk, q_len, kv_len, off, nmax;
+  int64_t tok0;  // token index of the sequence's first query row
+  int nkv[kQTiles];   // key tiles per query tile; -1 = the tile has no query rows
+  int row0[kQTiles];  // first query row of each tile within its sequence
+};
+
+template <bool PAGED>
+__device__ __forceinline__ int count_units(const PrefillParams& p) {
+  if constexpr (PAGED) {
+    return *p.work_count * p.Hq;
+  } else {
+    return ((p.S + 2 * kBM - 1) / (2 * kBM)) * p.B * p.Hq;
+  }
+}
+
+// Unit u in the global order (paged: the order of the device-built work list; dense: below).
+template <bool PAGED>
+__device__ __forceinline__ void unit_at(const PrefillParams& p, int u, Unit& w) {
+  int qt2;
+  if constexpr (PAGED) {
+    const int item = u / p.Hq;
+    w.h = u % p.Hq;
+    const int2 it = p.work_list[item];
+    w.seq = it.x;
+    qt2 = it.y;
+    const int c0 = p.cu_seqlens_q[w.seq], c1 = p.cu_seqlens_q[w.seq + 1];
+    w.tok0 = c0;
+    w.q_len = c1 - c0;
+    w.kv_len = min(p.kv_lens[w.seq], p.max_pages_per_seq * p.page_size);
+  } else {
+    // Units are grouped by chunks of kv heads sized so that one chunk is about one wave of CTAs:
+    // CTAs running together then read the K/V of only a few heads, which stay in L2 while every
+    // query tile of those heads streams them. Inside a chunk: query tiles heaviest first (causal),
+    // and for each tile the query heads of the chunk, those sharing a kv head adjacent.
+    const int T = (p.S + 2 * kBM - 1) / (2 * kBM);
+    const int G = p.group;
+    const int NKV = p.B * p.Hkv;
+    const int per_chunk = p.kv_heads_per_chunk * G * T;
+    const int chunk = u / per_chunk;
+    const int kv0 = chunk * p.kv_heads_per_chunk;
+    const int width = min(p.kv_heads_per_chunk, NKV - kv0) * G;  // query heads in this chunk
+    const int r = u - chunk * per_chunk;
+    qt2 = p.causal ? (T - 1 - r / width) : (r / width);
+    const int idx = r % width;
+    const int kvh = kv0 + idx / G;
+    w.seq = kvh / p.Hkv;
+    w.h = (kvh % p.Hkv) * G + idx % G;
+    w.tok0 = (int64_t)w.seq * p.S;
+    w.q_len = p.S;
+    w.kv_len = p.S;
+  }
+  w.hk = w.h / p.group;
+  w.off = w.kv_len - w.q_len;  // bottom-right causal alignment
+  w.nmax = 0;
+#pragma unroll
+  for (int g = 0; g < kQTiles; ++g) {
+    w.row0[g] = qt2 * (2 * kBM) + g * kBM;
+    if (w.row0[g] >= w.q_len) {
+      w.nkv[g] = -1;
+    } else {
+      const int last = min(w.row0[g] + kBM - 1, w.q_len - 1);
+      const int lim = p.causal ? min(w.kv_len, last + w.off + 1) : w.kv_len;
+      w.nkv[g] = lim > 0 ? (lim + kBN - 1) / kBN : 0;
+    }
+    w.nmax = max(w.nmax, w.nkv[g]);
+  }
+}
+
+// S = Q K^T for one 128x128 tile: D/16 MMAs of K = 16. Shared-memory descriptors are built once
+// by the caller; a K step only moves the start address, whose field (address >> 4, bits 0-13)
+// never carries into the next field inside the CTA's shared memory, so each step adds a
+// compile-time constant: 32 bytes inside a 128-byte swizzle row, and every 4 steps the next
+// 16 KB column block.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)((kk >> 2) * (Cfg<D>::kSubBytes >> 4) + (kk & 3) * 2);
+    mma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V for one tile: P (bf16 pairs) from TMEM as A, V as the MN-major B operand; a K step
+// of 16 keys is 16 rows of 128 bytes (2048 bytes) in each 64-column block of d, and P's 16 keys
+// are 8 TMEM columns.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    mma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)kk * (2048 >> 4), idesc, kk > 0 ? 1u : accumulate);
+}
+
+// Softmax numerators for 32-column chunks [C0, C0 + NC) of one score row held in registers:
+// p = 2^(s * sl2 - m) with the affine step and the row sum on fp32 pairs, P packed to bf16 pairs
+// and written to TMEM over the chunk's S columns (16 columns per chunk). Returns the chunks'
+// partial row sum as two fp32 halves of a pair.
+template <int C0, int NC>
+__device__ __forceinline__ uint64_t softmax_chunks(const uint32_t* sr, float sl2, float neg_m, uint32_t tS) {
+  const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
+  uint64_t ls4[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int cc = C0; cc < C0 + NC; ++cc) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = cc * 32 + 2 * i;
+      float x0, x1;
+      split_f32x2(fma_f32x2(f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      ls4[i & 3] = add_f32x2(ls4[i & 3], f32x2(p0, p1));
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(tS + cc * 16, pk);
+  }
+  return add_f32x2(add_f32x2(ls4[0], ls4[1]), add_f32x2(ls4[2], ls4[3]));
+}
+
+// Row max of 32-column chunks [C0, C0 + NC): four independent chains of three-input max.
+template <int C0, int NC>
+__device__ __forceinline__ float row_max_chunks(const uint32_t* sr) {
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = C0 * 32; c < (C0 + NC) * 32; c += 2)
+    mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+  return max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+}
+
+// Persistent schedule: CTA c takes units c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the
+// heaviest-first order, so every CTA gets a similar share of heavy and light units).
+__device__ __forceinline__ int unit_of_round(int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
 
 template <int D, bool PAGED>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -66,71 +206,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   uint8_t* sQ = smem;                  // kQTiles tiles
   uint8_t* sKV = smem + kQTiles * TB;  // NS stages
 
-  __shared__ uint64_t bar_q[kQTiles], bar_full[NS], bar_empty[NS];
-  __shared__ uint64_t bar_s[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_drain;
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_full[NS], bar_empty[NS];
+  __shared__ uint64_t bar_s[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_o_free[kQTiles], bar_drain[kQTiles];
+  __shared__ uint64_t bar_turn[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_units = count_units<PAGED>(p);
+  if ((int)blockIdx.x >= n_units) return;  // the grid is an upper bound
 
-  // ------------------------------------------------------------------ work unit
-  int seq, h, qt2, q_len, kv_len;
-  int64_t tok0;  // token index of the sequence's first query row
-  if constexpr (PAGED) {
-    const int item = blockIdx.x / p.Hq;
-    h = blockIdx.x % p.Hq;
-    if (item >= *p.work_count) return;  // grid is an upper bound on the number of items
-    const int2 w = p.work_list[item];
-    seq = w.x;
-    qt2 = w.y;
-    const int c0 = p.cu_seqlens_q[seq], c1 = p.cu_seqlens_q[seq + 1];
-    tok0 = c0;
-    q_len = c1 - c0;
-    kv_len = p.kv_lens[seq];
-  } else {
-    const int bh_count = p.B * p.Hq;
-    const int n2 = (p.S + 2 * kBM - 1) / (2 * kBM);
-    const int x = blockIdx.x;
-    // causal work is heaviest for the last query tiles: launch those first
-    qt2 = p.causal ? (n2 - 1 - x / bh_count) : (x / bh_count);
-    const int bh = x % bh_count;
-    seq = bh / p.Hq;
-    h = bh % p.Hq;
-    tok0 = (int64_t)seq * p.S;
-    q_len = p.S;
-    kv_len = p.S;
-  }
-  const int hk = h / p.group;
-  const int off = kv_len - q_len;  // bottom-right causal alignment
-  int nkv[kQTiles], row0[kQTiles];
-  int nmax = 0;
-#pragma unroll
-  for (int g = 0; g < kQTiles; ++g) {
-    row0[g] = qt2 * (2 * kBM) + g * kBM;
-    if (row0[g] >= q_len) {
-      nkv[g] = -1;  // no query rows in this tile
-    } else {
-      const int last = min(row0[g] + kBM - 1, q_len - 1);
-      const int lim = p.causal ? min(kv_len, last + off + 1) : kv_len;
-      nkv[g] = lim > 0 ? (lim + kBN - 1) / kBN : 0;
-    }
-    nmax = max(nmax, nkv[g]);
-  }
-
-  // ------------------------------------------------------------------ setup
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, kQTiles);  // one arrival per MMA issuer
+#pragma unroll
     for (int g = 0; g < kQTiles; ++g) {
-      mbar_init(&bar_q[g], 1);
       mbar_init(&bar_s[g], 1);
       mbar_init(&bar_p[g], 4 * 32);
       mbar_init(&bar_o[g], 1);
+      mbar_init(&bar_o_free[g], 4 * 32);
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], kQTiles);  // one arrival per MMA issuer
     }
-    mbar_init(&bar_drain, 1);
+    for (int g = 0; g < kQTiles; ++g) mbar_init(&bar_drain[g], 1);
+    mbar_init(&bar_turn[0], 1);
+    mbar_init(&bar_turn[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -144,159 +247,236 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   volatile int* abort = &abort_flag;
 
   if (warp == 0) {
+    regs_dec<kRegsControl>();
     // ================================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      for (int g = 0; g < kQTiles; ++g) {
-        if (nkv[g] <= 0) continue;
-        mbar_arrive_expect_tx(&bar_q[g], TB);
-        const int qrow = PAGED ? (int)(tok0 + row0[g]) : row0[g];
-        const int qbat = PAGED ? 0 : seq;
-#pragma unroll
-        for (int sub = 0; sub < C::kSub; ++sub)
-          tma_load_4d(sQ + g * TB + sub * C::kSubBytes, &p.tm_q, &bar_q[g], sub * 64, h, qrow, qbat);
-      }
     }
     const uint64_t kv_policy = policy_evict_last();
-    for (int idx = 0; idx < 2 * nmax; ++idx) {
-      const int j = idx >> 1;
-      const bool is_v = idx & 1;
-      const int stage = idx % NS;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&bar_empty[stage], ((idx / NS) & 1) ^ 1, abort, p.status, kSiteProducerEmpty);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      uint8_t* dst = sKV + stage * TB;
-      const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
-      if (lane == 0) mbar_arrive_expect_tx(&bar_full[stage], TB);
-      __syncwarp();
-      if constexpr (!PAGED) {
-        if (lane == 0) {
-#pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub)
-            tma_load_4d_hint(dst + sub * C::kSubBytes, tm, &bar_full[stage], sub * 64, hk, j * kBN, seq, kv_policy);
-        }
-      } else {
-        const int ppt = kBN / p.page_size;  // pages per tile
-        if (lane < ppt) {
-          const int lp = j * ppt + lane;    // logical page of this sequence
-          int phys = p.num_pages;           // past the pool: TMA fills zeros
-          if (lp * p.page_size < kv_len && lp < p.max_pages_per_seq)
-            phys = p.page_table[(int64_t)seq * p.max_pages_per_seq + lp];
-#pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub)
-            tma_load_4d_hint(dst + sub * C::kSubBytes + lane * p.page_size * 128, tm, &bar_full[stage], sub * 64,
-                             hk, 0, phys, kv_policy);
-        }
-      }
-      __syncwarp();
-    }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    const uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false);
-    const uint32_t idesc_pv = make_idesc_bf16(kBM, D, true);
-    const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-    // K-major operands (Q, K): 16-element K steps advance 32 bytes inside a 128-byte swizzle row,
-    // and every 4 steps move to the next 16 KB column block.
-    auto kmaj = [&](uint32_t base, int kk) {
-      return make_sdesc_sw128(base + (kk >> 2) * C::kSubBytes + (kk & 3) * 32, 16, 1024);
-    };
-    // V as the MN-major B operand of P V: 16 keys = 16 rows of 128 bytes per K step; the two
-    // 64-column blocks of d sit 16 KB apart (leading-dimension offset).
-    auto vmaj = [&](uint32_t base, int kk) { return make_sdesc_sw128(base + kk * 2048, C::kSubBytes, 1024); };
-
-    if (lane == 0) {
-      for (int g = 0; g < kQTiles; ++g)
-        if (nkv[g] > 0) mbar_wait(&bar_q[g], 0, abort, p.status, kSiteMmaQ);
-    }
-    if (nmax > 0) {
+    const uint64_t q_policy = policy_evict_first();
+    uint32_t kv_it = 0;  // position in the K/V ring, continued across units
+    for (int r = 0;; ++r) {
+      const int u = unit_of_round(r);
+      if (u >= n_units) break;
+      Unit w;
+      unit_at<PAGED>(p, u, w);
       if (lane == 0) {
-        mbar_wait(&bar_full[0], 0, abort, p.status, kSiteMmaFull);
-        tc_fence_after();
-        for (int g = 0; g < kQTiles; ++g) {
-          if (nkv[g] <= 0) continue;
+        // the previous unit's last Q K^T must have read the Q tiles before they are replaced
+        if (r > 0) mbar_wait(&bar_q_empty, (r - 1) & 1, abort, p.status, kSiteProducerEmpty);
+        int n_active = 0;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + g * 128, kmaj(sQa + g * TB, kk), kmaj(sKVa, kk), idesc_s, kk > 0);
-          mma_commit(&bar_s[g]);
+        for (int g = 0; g < kQTiles; ++g) n_active += w.nkv[g] > 0;
+        mbar_arrive_expect_tx(&bar_q_full, n_active * TB);
+#pragma unroll
+        for (int g = 0; g < kQTiles; ++g) {
+          if (w.nkv[g] <= 0) continue;
+          const int qrow = PAGED ? (int)(w.tok0 + w.row0[g]) : w.row0[g];
+          const int qbat = PAGED ? 0 : w.seq;
+#pragma unroll
+          for (int sub = 0; sub < C::kSub; ++sub)
+            tma_load_4d_hint(sQ + g * TB + sub * C::kSubBytes, &p.tm_q, &bar_q_full, sub * 64, w.h, qrow, qbat,
+                             q_policy);
         }
-        mma_commit(&bar_empty[0]);
       }
-      for (int j = 0; j < nmax; ++j) {
-        const int vi = 2 * j + 1, ki = 2 * j + 2;
-        const int vs = vi % NS, ks = ki % NS;
-        const bool has_next = j + 1 < nmax;
-        if (lane == 0) {
-          mbar_wait(&bar_full[vs], (vi / NS) & 1, abort, p.status, kSiteMmaFull);
-          if (has_next) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
+      __syncwarp();
+      for (int idx = 0; idx < 2 * w.nmax; ++idx, ++kv_it) {
+        const int j = idx >> 1;
+        const bool is_v = idx & 1;
+        const int stage = kv_it % NS;
+        if (lane == 0) mbar_wait(&bar_empty[stage], ((kv_it / NS) & 1) ^ 1, abort, p.status, kSiteProducerEmpty);
+        __syncwarp();
+        uint8_t* dst = sKV + stage * TB;
+        const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
+        if (lane == 0) mbar_arrive_expect_tx(&bar_full[stage], TB);
+        __syncwarp();
+        if constexpr (!PAGED) {
+          if (lane == 0) {
+#pragma unroll
+            for (int sub = 0; sub < C::kSub; ++sub)
+              tma_load_4d_hint(dst + sub * C::kSubBytes, tm, &bar_full[stage], sub * 64, w.hk, j * kBN, w.seq,
+                               kv_policy);
+          }
+        } else {
+          const int ppt = kBN / p.page_size;  // pages per tile
+          if (lane < ppt) {
+            const int lp = j * ppt + lane;    // logical page of this sequence
+            int phys = p.num_pages;           // past the pool: TMA fills zeros
+            if (lp * p.page_size < w.kv_len) phys = p.page_table[(int64_t)w.seq * p.max_pages_per_seq + lp];
+#pragma unroll
+            for (int sub = 0; sub < C::kSub; ++sub)
+              tma_load_4d_hint(dst + sub * C::kSubBytes + lane * p.page_size * 128, tm, &bar_full[stage],
+                               sub * 64, w.hk, 0, phys, kv_policy);
+          }
         }
         __syncwarp();
-        if constexpr (PAGED) {
-          // Rows of the sequence's partial last page past kv_len hold no valid value (possibly
-          // not even a finite one); P is 0 there but 0 * NaN is NaN, so they are zeroed first.
-          const int t0 = j * kBN;
-          if (t0 < kv_len && kv_len < t0 + kBN && (kv_len % p.page_size) != 0) {
-            const int r_begin = kv_len - t0;
-            const int r_end = min(kBN, ((kv_len + p.page_size - 1) / p.page_size) * p.page_size - t0);
-            uint8_t* vt = sKV + vs * TB;
-            const int n_chunks = (r_end - r_begin) * C::kSub * 8;  // 16-byte chunks
-            for (int c = lane; c < n_chunks; c += 32) {
-              const int row = r_begin + c / (C::kSub * 8);
-              const int sub = (c / 8) % C::kSub;
-              *reinterpret_cast<uint4*>(vt + sub * C::kSubBytes + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    regs_dec<kRegsControl>();
+    // ================================================================ MMA issuers
+    // Warp 1 issues every MMA of query tile 0, warp 2 those of query tile 1, taking turns (below).
+    // With two issuers one warp's waits and commits overlap the other's MMA issue; a single issuer
+    // serialises them and leaves the tensor core idle in between. Each K/V stage is released by
+    // one commit from each issuer (its empty barrier counts two arrivals).
+    const int g = warp - 1;
+    const uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false);
+    const uint32_t idesc_pv = make_idesc_bf16(kBM, D, true);
+    // Shared-memory descriptors are built once (see issue_qk / issue_pv for the K steps).
+    // V is the MN-major B operand of P V: the two 64-column blocks of d sit 16 KB apart.
+    const uint64_t dq = make_sdesc_sw128(smem_u32(sQ + g * TB), 16, 1024);
+    const uint64_t dk = make_sdesc_sw128(smem_u32(sKV), 16, 1024);
+    const uint64_t dv = make_sdesc_sw128(smem_u32(sKV), C::kSubBytes, 1024);
+    const uint32_t tS = tmem + g * 128, tO = tmem + C::kColO + g * D;
+    uint32_t kv_it = 0;   // ring position (K_j at kv_it + 2j, V_j at kv_it + 2j + 1)
+    uint32_t tcnt = 0;    // key tiles of this query tile so far (bar_s / bar_p phases)
+    uint32_t ounits = 0;  // units whose O this tile has produced (bar_o / bar_o_free phases)
+    // The issuers take turns (0, 1, 0, 1, ...) and issue a step's MMAs only on their turn. That
+    // keeps the tensor core's work in the order P0 V, Q0 K^T, P1 V, Q1 K^T, ...: one tile's
+    // softmax runs while the tensor core serves the other tile. Without turns the two tiles drift
+    // into lockstep, both softmaxes run at once and the tensor core idles meanwhile. Each issuer
+    // takes the same number of turns per unit (one for the first Q K^T, one per key tile).
+    uint32_t turn = 0;
+    auto take_turn = [&]() {
+      if (g == 0) {
+        if (turn > 0) mbar_wait(&bar_turn[0], (turn - 1) & 1, abort, p.status, kSiteMmaTurn);
+      } else {
+        mbar_wait(&bar_turn[1], turn & 1, abort, p.status, kSiteMmaTurn);
+      }
+    };
+    auto pass_turn = [&]() {
+      mbar_arrive(&bar_turn[1 - g]);
+      ++turn;
+    };
+    for (int r = 0;; ++r) {
+      const int u = unit_of_round(r);
+      if (u >= n_units) break;
+      Unit w;
+      unit_at<PAGED>(p, u, w);
+      const int nkv = g == 0 ? w.nkv[0] : w.nkv[1];
+      if (lane == 0) {
+        mbar_wait(&bar_q_full, r & 1, abort, p.status, kSiteMmaQ);
+        if (nkv <= 0) mma_commit(&bar_q_empty);  // this tile reads no Q this unit
+      }
+      if (w.nmax > 0) {
+        if (lane == 0) {
+          const int ks0 = kv_it % NS;
+          // Every issuer waits for a stage's fill before it arrives on the stage's empty barrier,
+          // also when its tile does not read the stage: an issuer can then never arrive twice on
+          // one pending phase, because the next fill waits for that phase to complete.
+          mbar_wait(&bar_full[ks0], (kv_it / NS) & 1, abort, p.status, kSiteMmaFull);
+          take_turn();
+          if (nkv > 0) {
+            tc_fence_after();
+            issue_qk<D>(tS, dq, dk + ks0 * (TB >> 4), idesc_s);
+          }
+          pass_turn();
+          if (nkv > 0) {
+            mma_commit(&bar_s[g]);
+            if (nkv == 1) mma_commit(&bar_q_empty);  // the unit's last Q K^T of this tile
+          }
+          mma_commit(&bar_empty[ks0]);
+        }
+        for (int j = 0; j < w.nmax; ++j) {
+          const uint32_t vi = kv_it + 2 * j + 1, ki = kv_it + 2 * j + 2;
+          const int vs = vi % NS, ks = ki % NS;
+          const bool has_next = j + 1 < w.nmax;
+          if (lane == 0) mbar_wait(&bar_full[vs], (vi / NS) & 1, abort, p.status, kSiteMmaFull);
+          __syncwarp();
+          bool turn_open = false;
+          if (j < nkv) {
+            if constexpr (PAGED) {
+              // Rows of the sequence's partial last page past kv_len hold no valid value (possibly
+              // not even a finite one); P is 0 there but 0 * NaN is NaN, so they are zeroed first.
+              // Both issuers write the same zeros, each before its own P V.
+              const int t0 = j * kBN;
+              if (t0 < w.kv_len && w.kv_len < t0 + kBN && (w.kv_len % p.page_size) != 0) {
+                const int r_begin = w.kv_len - t0;
+                const int r_end = min(kBN, ((w.kv_len + p.page_size - 1) / p.page_size) * p.page_size - t0);
+                uint8_t* vt = sKV + vs * TB;
+                const int n_chunks = (r_end - r_begin) * C::kSub * 8;  // 16-byte chunks
+                for (int c = lane; c < n_chunks; c += 32) {
+                  const int row = r_begin + c / (C::kSub * 8);
+                  const int sub = (c / 8) % C::kSub;
+                  *reinterpret_cast<uint4*>(vt + sub * C::kSubBytes + row * 128 + (c & 7) * 16) =
+                      make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+              }
+              __syncwarp();
             }
-            fence_proxy_async_smem();
+            if (lane == 0) {
+              mbar_wait(&bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
+              // the first P V of a unit overwrites O: the previous unit's O must have been read
+              if (j == 0 && ounits > 0) mbar_wait(&bar_o_free[g], (ounits - 1) & 1, abort, p.status, kSiteMmaP);
+              if (j + 1 < nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
+              take_turn();
+              turn_open = true;
+              tc_fence_after();
+              issue_pv<D>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
+              if (j + 1 < nkv) issue_qk<D>(tS, dq, dk + ks * (TB >> 4), idesc_s);
+              pass_turn();
+              if (j == nkv - 1) {
+                mma_commit(&bar_o[g]);
+                ++ounits;
+              }
+              if (j + 1 < nkv) {
+                mma_commit(&bar_s[g]);
+                if (j + 2 == nkv) mma_commit(&bar_q_empty);  // the unit's last Q K^T of this tile
+              }
+            }
+            ++tcnt;
+          }
+          if (lane == 0) {
+            if (!turn_open) {  // no MMA of this tile this step: still hand the turn on
+              take_turn();
+              pass_turn();
+            }
+            mma_commit(&bar_empty[vs]);
+            if (has_next) {
+              if (j + 1 >= nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
+              mma_commit(&bar_empty[ks]);
+            }
           }
           __syncwarp();
         }
-        if (lane == 0) {
-          tc_fence_after();
-          for (int g = 0; g < kQTiles; ++g) {
-            if (j >= nkv[g]) continue;
-            mbar_wait(&bar_p[g], j & 1, abort, p.status, kSiteMmaP);
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tmem + C::kColO + g * D, tmem + g * 128 + kk * 8, vmaj(sKVa + vs * TB, kk), idesc_pv,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-            if (j == nkv[g] - 1) mma_commit(&bar_o[g]);
-            if (j + 1 < nkv[g]) {
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(tmem + g * 128, kmaj(sQa + g * TB, kk), kmaj(sKVa + ks * TB, kk), idesc_s, kk > 0);
-              mma_commit(&bar_s[g]);
-            }
-          }
-          mma_commit(&bar_empty[vs]);
-          if (has_next) mma_commit(&bar_empty[ks]);
-        }
-        __syncwarp();
+        kv_it += 2 * w.nmax;
       }
+      __syncwarp();
     }
-    // drain: every MMA this CTA issued has completed before TMEM is released
+    // drain: every MMA this warp issued has completed before TMEM is released
     if (lane == 0) {
-      mma_commit(&bar_drain);
+      mma_commit(&bar_drain[g]);
       int no_abort = 0;
-      mbar_wait(&bar_drain, 0, &no_abort, p.status, kSiteDrain);
+      mbar_wait(&bar_drain[g], 0, &no_abort, p.status, kSiteDrain);
     }
     __syncwarp();
+  } else if (warp == 3) {
+    regs_dec<kRegsControl>();
   } else if (warp >= 4) {
+    regs_inc<kRegsSoftmax>();
     // ================================================================ softmax warpgroups
     const int g = (warp - 4) >> 2;
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = wq * 32 + lane;
+    const int r_in = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + g * 128 + lane_off;
     const uint32_t tO = tmem + C::kColO + g * D + lane_off;
-    if (nkv[g] >= 0) {
-      const int row = row0[g] + r;
-      const int lim_row = p.causal ? min(kv_len, row + off + 1) : kv_len;  // keys [0, lim_row)
-      const float sl2 = p.scale_log2;
+    const float sl2 = p.scale_log2;
+    uint32_t tcnt = 0, ounits = 0;
+    for (int r = 0;; ++r) {
+      const int u = unit_of_round(r);
+      if (u >= n_units) break;
+      Unit w;
+      unit_at<PAGED>(p, u, w);
+      const int nkv = g == 0 ? w.nkv[0] : w.nkv[1];
+      if (nkv < 0) continue;
+      const int row = (g == 0 ? w.row0[0] : w.row0[1]) + r_in;
+      const int lim_row = p.causal ? min(w.kv_len, row + w.off + 1) : w.kv_len;  // keys [0, lim_row)
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < nkv[g]; ++j) {
-        mbar_wait(&bar_s[g], j & 1, abort, p.status, kSiteSoftmaxS);
+      for (int j = 0; j < nkv; ++j, ++tcnt) {
+        mbar_wait(&bar_s[g], tcnt & 1, abort, p.status, kSiteSoftmaxS);
         __syncwarp();  // lanes leave the wait at different times; tcgen05.ld is warp-collective
         tc_fence_after();
         uint32_t sr[kBN];
@@ -314,30 +494,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           for (int c = 0; c < kBN; ++c)
             if (c >= valid) sr[c] = 0xff800000u;  // -inf
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, u2f(sr[c]));
-        const float m_tile = mx * sl2;
-        float alpha = 1.f;
+        const float m_tile = row_max_chunks<0, 4>(sr) * sl2;
         const bool need = m_tile > m_run + kRescaleThreshold;
-        if (need) {
-          alpha = ex2(m_run - m_tile);  // 0 while m_run is -inf
-          m_run = m_tile;
-        }
-        l_run *= alpha;
-        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(u2f(sr[cc * 32 + 2 * i]), sl2, neg_m));
-            const float p1 = ex2(fmaf(u2f(sr[cc * 32 + 2 * i + 1]), sl2, neg_m));
-            l_run += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS + cc * 16, pk);
-        }
+        const float alpha = need ? ex2(m_run - m_tile) : 1.f;  // 0 while m_run is -inf
+        if (need) m_run = m_tile;
+        float la, lb;
+        split_f32x2(softmax_chunks<0, 4>(sr, sl2, m_run == -INFINITY ? 0.f : -m_run, tS), la, lb);
+        l_run = fmaf(l_run, alpha, la + lb);
         // O rescale (after P is written, so S no longer occupies registers): P V of the previous
         // tile is complete, because the commit that signalled this tile's S was issued after it.
         if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -356,37 +519,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         mbar_arrive(&bar_p[g]);
         __syncwarp();
       }
-      // ---------------------------------------------------------- epilogue: O / l, LSE
-      if (nkv[g] > 0) {
-        mbar_wait(&bar_o[g], 0, abort, p.status, kSiteSoftmaxO);
+      // ------------------------------------------------------------ epilogue: O / l, LSE
+      uint32_t orr[D];
+      if (nkv > 0) {
+        mbar_wait(&bar_o[g], ounits & 1, abort, p.status, kSiteSoftmaxO);
         __syncwarp();
         tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, orr + cc * 32);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(orr + cc * 32);
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[g]);  // the MMA may now overwrite O with the next unit
+        ++ounits;
+      } else {
+#pragma unroll
+        for (int i = 0; i < D; ++i) orr[i] = 0u;
       }
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      const int64_t tok = tok0 + row;
-      const bool store = row < q_len && (!PAGED || tok < p.total_q);
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * D;
+      const int64_t tok = w.tok0 + row;
+      const bool store = row < w.q_len && (!PAGED || tok < p.total_q);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + w.h) * D);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t orr[32];
-        if (nkv[g] > 0) {
-          tmem_ld32(tO + cc * 32, orr);
-          tmem_ld_wait(orr);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(orr[2 * i]) * inv_l, u2f(orr[2 * i + 1]) * inv_l);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        for (int i = 0; i < D / 8; ++i)
+          dst[i] = make_uint4(pack_bf16x2(u2f(orr[8 * i + 0]) * inv_l, u2f(orr[8 * i + 1]) * inv_l),
+                              pack_bf16x2(u2f(orr[8 * i + 2]) * inv_l, u2f(orr[8 * i + 3]) * inv_l),
+                              pack_bf16x2(u2f(orr[8 * i + 4]) * inv_l, u2f(orr[8 * i + 5]) * inv_l),
+                              pack_bf16x2(u2f(orr[8 * i + 6]) * inv_l, u2f(orr[8 * i + 7]) * inv_l));
+        if (p.lse != nullptr) p.lse[tok * p.Hq + w.h] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
       }
-      if (store && p.lse != nullptr)
-        p.lse[tok * p.Hq + h] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      __syncwarp();
     }
   }
 
@@ -398,50 +561,84 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   }
 }
 
-// Work list for the paged prefill: one item per (sequence, pair of query tiles), sorted by the
-// number of key tiles it streams, heaviest first (a counting sort over that cost).
+// Work list for the paged prefill: one item per (sequence, pair of query tiles). Sequences come
+// longest first (a counting sort on their key-tile count); the items of one sequence are
+// contiguous, heaviest query tiles first, so the CTAs running together share one sequence's
+// K/V pages in L2 while the order still starts with the longest work.
 __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ kv_lens,
                                   int num_seqs, int causal, int max_cost, int max_items,
-                                  int2* __restrict__ work_list, int* __restrict__ work_count) {
+                                  int2* __restrict__ work_list, int* __restrict__ work_count,
+                                  int* __restrict__ order) {
   extern __shared__ int hist[];  // max_cost + 1 buckets
   const int tid = threadIdx.x, nt = blockDim.x;
+  __shared__ int total;
   for (int c = tid; c <= max_cost; c += nt) hist[c] = 0;
   __syncthreads();
-  auto cost_of = [&](int q_len, int kv_len, int it) {
-    const int last = min(it * 2 * kBM + 2 * kBM - 1, q_len - 1);
-    const int lim = causal ? min(kv_len, last + (kv_len - q_len) + 1) : kv_len;
-    const int n = lim > 0 ? (lim + kBN - 1) / kBN : 0;
-    return min(n, max_cost);
+  auto cost_of = [&](int s) {
+    const int kv = kv_lens[s];
+    return min(kv > 0 ? (kv + kBN - 1) / kBN : 0, max_cost);
   };
-  for (int s = tid; s < num_seqs; s += nt) {
-    const int q_len = cu[s + 1] - cu[s], kv_len = kv_lens[s];
-    const int items = (q_len + 2 * kBM - 1) / (2 * kBM);
-    for (int it = 0; it < items; ++it) atomicAdd(&hist[cost_of(q_len, kv_len, it)], 1);
-  }
+  for (int s = tid; s < num_seqs; s += nt) atomicAdd(&hist[cost_of(s)], 1);
   __syncthreads();
   if (tid == 0) {
+    // bucket offsets, longest first; then a stable placement of every sequence, then item offsets
     int run = 0;
     for (int c = max_cost; c >= 0; --c) {
       const int t = hist[c];
       hist[c] = run;
       run += t;
     }
-    *work_count = min(run, max_items);  // more items than the host bound means inconsistent lengths
+    for (int s = 0; s < num_seqs; ++s) order[hist[cost_of(s)]++] = s;
+    int items = 0;
+    for (int k = 0; k < num_seqs; ++k) {
+      const int s = order[k];
+      const int q_len = cu[s + 1] - cu[s];
+      order[num_seqs + k] = items;  // first item of the k-th sequence in the order
+      items += q_len > 0 ? (q_len + 2 * kBM - 1) / (2 * kBM) : 0;
+    }
+    total = min(items, max_items);  // more items than the host bound means inconsistent lengths
+    *work_count = total;
   }
   __syncthreads();
-  for (int s = tid; s < num_seqs; s += nt) {
-    const int q_len = cu[s + 1] - cu[s], kv_len = kv_lens[s];
-    const int items = (q_len + 2 * kBM - 1) / (2 * kBM);
-    for (int it = 0; it < items; ++it) {
-      const int pos = atomicAdd(&hist[cost_of(q_len, kv_len, it)], 1);
-      if (pos < max_items) work_list[pos] = make_int2(s, it);
+  for (int k = tid; k < num_seqs; k += nt) {
+    const int s = order[k];
+    const int q_len = cu[s + 1] - cu[s];
+    const int n = q_len > 0 ? (q_len + 2 * kBM - 1) / (2 * kBM) : 0;
+    const int base = order[num_seqs + k];
+    for (int it = 0; it < n; ++it) {
+      const int pos = base + it;
+      if (pos < total) work_list[pos] = make_int2(s, causal ? n - 1 - it : it);
     }
   }
+}
+
+// Grid size: by default one CTA per work unit, issued in unit order by the hardware scheduler
+// (which assigns units to SMs as they free up); FA_PREFILL_PERSISTENT=1 selects one CTA per SM
+// looping over units in the snake order.
+bool persistent_grid() {
+  static int mode = -1;
+  if (mode < 0) {
+    const char* e = getenv("FA_PREFILL_PERSISTENT");
+    mode = (e != nullptr && e[0] == '1') ? 1 : 0;
+  }
+  return mode == 1;
 }
 
 template <int D, bool PAGED>
 cudaError_t launch_prefill_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   auto kern = prefill_kernel<D, PAGED>;
+  {
+    // The register split (kRegsControl / kRegsSoftmax) draws on the registers the CTA launches
+    // with; a larger split would make the increase wait forever, so refuse to launch instead.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+      cudaFuncAttributes attr;
+      const cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+      if (e != cudaSuccess) return e;
+      launch_regs = attr.numRegs;
+    }
+    if (128 * kRegsControl + 256 * kRegsSoftmax > kPrefillThreads * launch_regs) return cudaErrorInvalidConfiguration;
+  }
   static int configured_mask = 0;  // one bit per device ordinal below 32
   int dev = 0;
   cudaGetDevice(&dev);
@@ -456,21 +653,24 @@ cudaError_t launch_prefill_impl(const PrefillParams& p, int grid, cudaStream_t s
 
 }  // namespace
 
-cudaError_t launch_prefill_dense(const PrefillParams& p, int d, cudaStream_t stream) {
+cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cudaStream_t stream) {
   const int n2 = (p.S + 2 * kBM - 1) / (2 * kBM);
-  const int grid = n2 * p.B * p.Hq;
+  const long long units = (long long)n2 * p.B * p.Hq;
+  const int grid = (int)((units < sm_count || !persistent_grid()) ? units : sm_count);
   if (d == 128) return launch_prefill_impl<128, false>(p, grid, stream);
   return launch_prefill_impl<64, false>(p, grid, stream);
 }
 
-cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int max_items, int max_kv_tiles, int2* work_list,
-                                 int* work_count, cudaStream_t stream) {
+cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
+                                 int2* work_list, int* work_count, cudaStream_t stream) {
   const int smem = (max_kv_tiles + 1) * (int)sizeof(int);
+  int* order = reinterpret_cast<int*>(work_list + max_items);  // 2 * num_seqs ints of scratch
   plan_paged_kernel<<<1, 1024, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, max_kv_tiles,
-                                              max_items, work_list, work_count);
+                                              max_items, work_list, work_count, order);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int grid = max_items * p.Hq;
+  const long long units = (long long)max_items * p.Hq;
+  const int grid = (int)((units < sm_count || !persistent_grid()) ? units : sm_count);
   if (d == 128) return launch_prefill_impl<128, true>(p, grid, stream);
   return launch_prefill_impl<64, true>(p, grid, stream);
 }

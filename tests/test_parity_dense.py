@@ -37,6 +37,8 @@ CASES = [
     (1, 777, 4, 1, 64, True),
     (3, 640, 2, 2, 128, False),
     (1, 2048, 2, 2, 128, True),
+    (2, 2048, 16, 16, 128, True),  # head chunks of the persistent schedule, the last one partial
+    (1, 1024, 24, 8, 64, False),   # several rounds of the persistent schedule, GQA 3
 ]
 
 
