@@ -46,6 +46,13 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
   }
 }
 
+// bf16 x 8 -> four fp32 pairs (element 2i in the low half of pair i)
+__device__ __forceinline__ void bf16x8_to_f32x2(const uint4 u, uint64_t* f2) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f2[i] = f32x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, int n_stages) {
@@ -122,25 +129,28 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
   const int rg = lane / C::LPR;  // row within a step
   const int lr = lane % C::LPR;  // lane within the row
   const int tok = q_begin;       // the single query token of this sequence
-  float qf[G][C::EPL];
+  // q and the output accumulator are held as fp32 pairs for the paired .f32x2 instructions
+  uint64_t qf2[G][C::EPL / 2];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const int h = hk * G + g;
     const uint4* qp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)tok * p.Hq + h) * D);
 #pragma unroll
     for (int c = 0; c < C::CPL; ++c) {
-      bf16x8_to_f32(qp[lr + c * C::LPR], &qf[g][c * 8]);
+      float t[8];
+      bf16x8_to_f32(qp[lr + c * C::LPR], t);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qf[g][c * 8 + e] *= p.scale_log2;
+      for (int e = 0; e < 4; ++e) qf2[g][c * 4 + e] = f32x2(t[2 * e] * p.scale_log2, t[2 * e + 1] * p.scale_log2);
     }
   }
-  float m[G], l[G], o[G][C::EPL];
+  float m[G], l[G];
+  uint64_t o2[G][C::EPL / 2];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
 #pragma unroll
-    for (int e = 0; e < C::EPL; ++e) o[g][e] = 0.f;
+    for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = 0ull;
   }
 
   for (int i = 0; i < n_mine; ++i) {
@@ -154,14 +164,17 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
     for (int it = 0; it < C::ITERS; ++it) {
       const int r = it * C::RPI + rg;
       const uint4* kp = reinterpret_cast<const uint4*>(sk + ((size_t)r * hpc + warp) * D * 2);
-      float kf[C::EPL];
+      uint64_t kf2[C::EPL / 2];
 #pragma unroll
-      for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32(kp[lr + c * C::LPR], &kf[c * 8]);
+      for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32x2(kp[lr + c * C::LPR], &kf2[c * 4]);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
+        uint64_t acc2 = 0ull;
 #pragma unroll
-        for (int e = 0; e < C::EPL; ++e) acc = fmaf(qf[g][e], kf[e], acc);
+        for (int e = 0; e < C::EPL / 2; ++e) acc2 = fma_f32x2(qf2[g][e], kf2[e], acc2);
+        float a0, a1;
+        split_f32x2(acc2, a0, a1);
+        float acc = a0 + a1;
 #pragma unroll
         for (int sh = 1; sh < C::LPR; sh <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
         sc[it][g] = (row_base + r < kv_len) ? acc : -INFINITY;
@@ -179,8 +192,9 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
       if (m_new > m[g]) {
         const float alpha = ex2(m[g] - m_new);  // 0 while m is -inf
         l[g] *= alpha;
+        const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < C::EPL; ++e) o[g][e] *= alpha;
+        for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = mul_f32x2(o2[g][e], a2);
         m[g] = m_new;
       }
       const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
@@ -194,15 +208,17 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
     for (int it = 0; it < C::ITERS; ++it) {
       const int r = it * C::RPI + rg;
       const uint4* vp = reinterpret_cast<const uint4*>(sv + ((size_t)r * hpc + warp) * D * 2);
-      float vf[C::EPL];
+      uint64_t vf2[C::EPL / 2];
 #pragma unroll
-      for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32(vp[lr + c * C::LPR], &vf[c * 8]);
+      for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32x2(vp[lr + c * C::LPR], &vf2[c * 4]);
       // rows past kv_len carry p = 0; their V may be arbitrary bits, so they are skipped
       if (row_base + r < kv_len) {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) {
+          const uint64_t p2 = f32x2(sc[it][g], sc[it][g]);
 #pragma unroll
-          for (int e = 0; e < C::EPL; ++e) o[g][e] = fmaf(sc[it][g], vf[e], o[g][e]);
+          for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = fma_f32x2(p2, vf2[e], o2[g][e]);
+        }
       }
     }
     __syncwarp();
@@ -212,6 +228,11 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
       if (mbar_wait(&bar_empty[s], (i / n_stages) & 1, abort, p.status, kSiteDecodeEmpty)) issue(i + n_stages);
     }
   }
+  float o[G][C::EPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < C::EPL / 2; ++e) split_f32x2(o2[g][e], o[g][2 * e], o[g][2 * e + 1]);
 
   // combine the row groups of the warp (they share m): sum l and O over lanes lr + k * LPR
 #pragma unroll

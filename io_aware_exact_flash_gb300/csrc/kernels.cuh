@@ -32,6 +32,7 @@ struct alignas(64) PrefillParams {
   // dense
   int B, S;
   int kv_heads_per_chunk;  // unit order: kv heads whose query tiles are scheduled together
+  int pair_units;          // dense causal: each CTA takes query-tile pairs i and T-1-i of one head
   // paged
   const int32_t* page_table;
   const int32_t* cu_seqlens_q;

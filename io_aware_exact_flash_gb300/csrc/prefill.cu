@@ -195,6 +195,34 @@ __device__ __forceinline__ int unit_of_round(int r) {
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
+// Paired schedule (dense causal): CTA c takes two units of one query head, query-tile pair i
+// and its mirror T-1-i, heaviest first. Under causal masking every pair then costs the same, so
+// the hardware scheduler balances CTAs well, half as many CTAs start, and the second unit's
+// prologue overlaps the first unit's tail. Returns a unit index of the dense order (unit_at), or
+// n_units when the CTA has no unit for this round.
+template <bool PAGED>
+__device__ __forceinline__ int unit_of_pair_round(const PrefillParams& p, int r, int n_units) {
+  if constexpr (PAGED) {
+    return n_units;
+  } else {
+    const int T = (p.S + 2 * kBM - 1) / (2 * kBM);
+    const int half = (T + 1) / 2;  // pairs per query head
+    const int G = p.group;
+    const int NKV = p.B * p.Hkv;
+    const int pairs_per_chunk = p.kv_heads_per_chunk * G * half;
+    const int c = blockIdx.x;
+    const int chunk = c / pairs_per_chunk;
+    const int kv0 = chunk * p.kv_heads_per_chunk;
+    const int width = min(p.kv_heads_per_chunk, NKV - kv0) * G;
+    const int rc = c - chunk * pairs_per_chunk;
+    const int i = rc / width, head = rc % width;
+    const int chunk_start = chunk * p.kv_heads_per_chunk * G * T;
+    if (r == 0) return chunk_start + i * width + head;                              // qt2 = T-1-i
+    if (r == 1 && T - 1 - i != i) return chunk_start + (T - 1 - i) * width + head;  // qt2 = i
+    return n_units;
+  }
+}
+
 template <int D, bool PAGED>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
@@ -214,7 +242,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_units = count_units<PAGED>(p);
-  if ((int)blockIdx.x >= n_units) return;  // the grid is an upper bound
+  if (!p.pair_units && (int)blockIdx.x >= n_units) return;  // the grid is an upper bound
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -258,7 +286,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const uint64_t q_policy = policy_evict_first();
     uint32_t kv_it = 0;  // position in the K/V ring, continued across units
     for (int r = 0;; ++r) {
-      const int u = unit_of_round(r);
+      const int u = p.pair_units ? unit_of_pair_round<PAGED>(p, r, n_units) : unit_of_round(r);
       if (u >= n_units) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
@@ -281,6 +309,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         }
       }
       __syncwarp();
+      // paged: lane l < 128 / page_size holds the physical id of page l of the current key tile;
+      // the ids of the next tile are fetched right after this tile's K boxes are issued, so the
+      // page-table read is off the path to the next TMA
+      const int ppt = PAGED ? kBN / p.page_size : 0;  // pages per key tile
+      auto page_id = [&](int tile) {
+        const int lp = tile * ppt + lane;  // logical page of this sequence
+        return lp * p.page_size < w.kv_len ? p.page_table[(int64_t)w.seq * p.max_pages_per_seq + lp]
+                                           : p.num_pages;  // past the pool: TMA fills zeros
+      };
+      int phys_cur = 0, phys_next = 0;
+      if (PAGED && lane < ppt && w.nmax > 0) phys_cur = page_id(0);
       for (int idx = 0; idx < 2 * w.nmax; ++idx, ++kv_it) {
         const int j = idx >> 1;
         const bool is_v = idx & 1;
@@ -299,15 +338,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                                kv_policy);
           }
         } else {
-          const int ppt = kBN / p.page_size;  // pages per tile
           if (lane < ppt) {
-            const int lp = j * ppt + lane;    // logical page of this sequence
-            int phys = p.num_pages;           // past the pool: TMA fills zeros
-            if (lp * p.page_size < w.kv_len) phys = p.page_table[(int64_t)w.seq * p.max_pages_per_seq + lp];
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub)
               tma_load_4d_hint(dst + sub * C::kSubBytes + lane * p.page_size * 128, tm, &bar_full[stage],
-                               sub * 64, w.hk, 0, phys, kv_policy);
+                               sub * 64, w.hk, 0, phys_cur, kv_policy);
+            if (!is_v) {
+              phys_next = page_id(j + 1);
+            } else {
+              phys_cur = phys_next;
+            }
           }
         }
         __syncwarp();
@@ -350,7 +390,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       ++turn;
     };
     for (int r = 0;; ++r) {
-      const int u = unit_of_round(r);
+      const int u = p.pair_units ? unit_of_pair_round<PAGED>(p, r, n_units) : unit_of_round(r);
       if (u >= n_units) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
@@ -466,7 +506,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const float sl2 = p.scale_log2;
     uint32_t tcnt = 0, ounits = 0;
     for (int r = 0;; ++r) {
-      const int u = unit_of_round(r);
+      const int u = p.pair_units ? unit_of_pair_round<PAGED>(p, r, n_units) : unit_of_round(r);
       if (u >= n_units) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
@@ -612,16 +652,18 @@ __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t*
   }
 }
 
-// Grid size: by default one CTA per work unit, issued in unit order by the hardware scheduler
-// (which assigns units to SMs as they free up); FA_PREFILL_PERSISTENT=1 selects one CTA per SM
-// looping over units in the snake order.
-bool persistent_grid() {
-  static int mode = -1;
-  if (mode < 0) {
+// Grid size. Dense causal: one CTA per pair of mirrored query-tile pairs (unit_of_pair_round);
+// dense non-causal: one CTA per unit. The hardware scheduler hands CTAs to SMs as they free up,
+// which measured faster than a persistent static order for dense work. Paged: one CTA per SM
+// looping over units in the snake order (measured faster there). The environment variable
+// FA_PREFILL_PERSISTENT=0 (one CTA per unit) or 1 (persistent) overrides both.
+int persistent_override() {
+  static int mode = -2;
+  if (mode == -2) {
     const char* e = getenv("FA_PREFILL_PERSISTENT");
-    mode = (e != nullptr && e[0] == '1') ? 1 : 0;
+    mode = (e == nullptr || (e[0] != '0' && e[0] != '1')) ? -1 : (e[0] == '1');
   }
-  return mode == 1;
+  return mode;  // -1: no override
 }
 
 template <int D, bool PAGED>
@@ -656,7 +698,19 @@ cudaError_t launch_prefill_impl(const PrefillParams& p, int grid, cudaStream_t s
 cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cudaStream_t stream) {
   const int n2 = (p.S + 2 * kBM - 1) / (2 * kBM);
   const long long units = (long long)n2 * p.B * p.Hq;
-  const int grid = (int)((units < sm_count || !persistent_grid()) ? units : sm_count);
+  const int mode = persistent_override();
+  int grid;
+  if (mode == 1) {
+    grid = (int)(units < sm_count ? units : sm_count);
+  } else if (mode == 0 || !p.causal) {
+    grid = (int)units;
+  } else {
+    PrefillParams q = p;  // causal: mirrored query-tile pairs, one pair per CTA
+    q.pair_units = 1;
+    grid = ((n2 + 1) / 2) * p.B * p.Hq;
+    if (d == 128) return launch_prefill_impl<128, false>(q, grid, stream);
+    return launch_prefill_impl<64, false>(q, grid, stream);
+  }
   if (d == 128) return launch_prefill_impl<128, false>(p, grid, stream);
   return launch_prefill_impl<64, false>(p, grid, stream);
 }
@@ -670,7 +724,8 @@ cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, in
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long units = (long long)max_items * p.Hq;
-  const int grid = (int)((units < sm_count || !persistent_grid()) ? units : sm_count);
+  const bool persistent = persistent_override() != 0;
+  const int grid = (int)((units < sm_count || !persistent) ? units : sm_count);
   if (d == 128) return launch_prefill_impl<128, true>(p, grid, stream);
   return launch_prefill_impl<64, true>(p, grid, stream);
 }
