@@ -149,6 +149,15 @@ fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages, const void
  */
 fa_status fa_get_device_status(fa_stream_t stream, int* code, int* site);
 
+/*
+ * Diagnostic of the device-side failure path: launches one warp that waits on a barrier phase
+ * nothing completes, with a wait limit of limit_ms (1..2000). The wait must give up, record
+ * FA_ERR_DEVICE_TIMEOUT in the device status word and let the kernel exit; nothing traps or
+ * hangs. Synchronises `stream`, then returns in *code (and *site, may be NULL) what the status
+ * word held, and clears it. Returns FA_OK when the check ran (inspect *code for its result).
+ */
+fa_status fa_selftest_wait_timeout(int limit_ms, int* code, int* site, fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

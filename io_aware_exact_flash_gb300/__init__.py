@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     fa_merge_states,
     fa_paged_decode_noalloc,
     fa_paged_fwd,
+    fa_selftest_wait_timeout,
     fa_paged_workspace_bytes,
     load_library,
     status_string,

@@ -24,7 +24,8 @@ _STATUS_NAMES = {
 }
 
 EXPORTED = ("fa_status_string", "fa_fwd", "fa_paged_fwd", "fa_paged_workspace_bytes",
-            "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status", "fa_paged_decode_noalloc")
+            "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status", "fa_paged_decode_noalloc",
+            "fa_selftest_wait_timeout")
 
 
 class FaError(RuntimeError):
@@ -66,6 +67,8 @@ def load_library(path: str = None) -> ctypes.CDLL:
     lib.fa_merge_states.restype = i
     lib.fa_paged_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp, vp, i, vp]
     lib.fa_paged_decode_noalloc.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [i, ctypes.POINTER(i), ctypes.POINTER(i), vp]
+    lib.fa_selftest_wait_timeout.restype = i
     lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i), ctypes.POINTER(i)]
     lib.fa_get_device_status.restype = i
     _lib = lib
@@ -219,3 +222,12 @@ def fa_paged_decode_noalloc(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_le
         _stream(stream))
     _check("fa_paged_decode_noalloc", code)
     return out, lse
+
+
+def fa_selftest_wait_timeout(limit_ms=50, stream=None):
+    """Runs the device-side timeout diagnostic; returns (code, site) the status word recorded."""
+    code, site = ctypes.c_int(0), ctypes.c_int(0)
+    _check("fa_selftest_wait_timeout",
+           load_library().fa_selftest_wait_timeout(int(limit_ms), ctypes.byref(code), ctypes.byref(site),
+                                                   _stream(stream)))
+    return code.value, site.value

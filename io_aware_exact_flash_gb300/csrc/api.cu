@@ -157,6 +157,23 @@ int sm_count_now() {
   return 148;
 }
 
+// Diagnostic: one warp waits on an mbarrier phase that nothing will ever complete. The bounded
+// wait must give up after limit_ns, record FA_ERR_DEVICE_TIMEOUT with the site id in the status
+// word and let the kernel exit normally.
+constexpr uint32_t kSiteSelftest = 99;
+
+__global__ void wait_timeout_selftest_kernel(DeviceStatus* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    fa::mbar_init(&bar, 1);
+    fa::fence_mbar_init();
+  }
+  __syncthreads();
+  fa::mbar_wait(&bar, 0, &abort_flag, status, kSiteSelftest, limit_ns);
+}
+
 }  // namespace
 
 int fa::current_device_info(DeviceStatus** status, int* sm_count) {
@@ -381,6 +398,19 @@ fa_status fa_get_device_status(fa_stream_t stream, int* code, int* site) {
   *code = (int)h.code;
   if (site) *site = (int)h.where;
   return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(int limit_ms, int* code, int* site, fa_stream_t stream) {
+  if (!code || limit_ms < 1 || limit_ms > 2000) return FA_ERR_INVALID_ARG;
+  fa_status err = FA_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+  int dummy = 0;
+  err = fa_get_device_status(stream, &dummy, nullptr);  // start from a clear status word
+  if (err != FA_OK) return err;
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(dev->status, (uint64_t)limit_ms * 1000000ull);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return fa_get_device_status(stream, code, site);
 }
 
 }  // extern "C"

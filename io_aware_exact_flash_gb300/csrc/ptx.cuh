@@ -25,6 +25,9 @@ struct DeviceStatus {
 
 // Wall-clock limit on any single wait (nanoseconds). A healthy pipeline never waits this long.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Backstop in case the global timer ever stalls: a wait also gives up after this many polls.
+// Each poll sleeps up to 100 us when the phase is pending, so this is far beyond kWaitLimitNs.
+constexpr uint32_t kWaitMaxPolls = 1u << 28;
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
@@ -72,11 +75,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Gives up after kWaitLimitNs: then it
+// Wait for the phase with the given parity to complete. Gives up after limit_ns: then it
 // records (code, site) in the device status word, sets *abort and returns false. Once *abort is
 // set (by any warp of the CTA) waits return at once, so every warp reaches the CTA's exit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          DeviceStatus* status, uint32_t site) {
+                                          DeviceStatus* status, uint32_t site,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
@@ -84,9 +88,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if ((it & 15u) == 0) {
       uint64_t t = global_timer_ns();
-      if (t0 == 0) {
-        t0 = t;
-      } else if (t - t0 > kWaitLimitNs) {
+      if (t0 == 0) t0 = t;
+      if (t - t0 > limit_ns || it >= kWaitMaxPolls) {
         *abort = 1;
         if (status) {
           atomicCAS(&status->code, 0u, 7u /* FA_ERR_DEVICE_TIMEOUT */);
