@@ -3,8 +3,9 @@
 One timed step is one forward pass of causal prefill attention over the workload the headline
 metric is quoted on (B=4, Hq=Hkv=32, S=4096, d=128, bf16, synthetic N(0,1) inputs). The same run
 also times, with the same step and warm-up counts, the other workloads of the hot path: long-context
-GQA prefill (S=32768), paged ragged prefill (64 sequences) and paged split-KV decode (128
-sequences); their numbers go to the "extra" object of the single JSON line rank 0 prints.
+GQA prefill (S=32768), paged ragged prefill (64 sequences), paged split-KV decode (128
+sequences) and the paged KV append that fills the prefill batch's cache; their numbers go to the
+"extra" object of the single JSON line rank 0 prints.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -33,6 +34,8 @@ if ROOT not in sys.path:
 
 from io_aware_exact_flash_gb300.workloads import (  # noqa: E402
     WORKLOADS,
+    make_append,
+    make_cascade,
     make_dense,
     make_paged,
     paged_allowed_scores,
@@ -41,7 +44,8 @@ from io_aware_exact_flash_gb300.workloads import (  # noqa: E402
 METRIC = "attn fwd TFLOP/s (prefill) & decode HBM GB/s on 1 GB300, % of roofline"
 HEADLINE = "causal_prefill_b4_h32_s4096_d128"
 EXTRAS = ["gqa_causal_prefill_b1_hq32_hkv8_s32768_d128", "paged_prefill_64seq_512_8192_hq32_hkv8_d128_p16",
-          "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16"]
+          "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16", "paged_append_64seq_512_8192_hkv8_d128_p16",
+          "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) of one headline prefill launch from the ncu capture summarised in
 # profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on; the
@@ -242,7 +246,99 @@ class PagedCase:
 
     @property
     def launches(self):
-        return 2 if (not self.w.decode or self.splits > 1) else 1
+        # prefill: the planning kernel and the attention kernel; decode: one kernel (the merge is
+        # fused into it; its counter reset is a cudaMemsetAsync, not a kernel)
+        return 1 if self.w.decode else 2
+
+
+class AppendCase:
+    """Paged KV append of a whole batch's K/V rows into their pages (the cache fill of the paged
+    prefill batch). Algorithmic bytes: every new K and V row read once and written once."""
+
+    def __init__(self, name, device):
+        import torch
+
+        self.w = WORKLOADS[name]
+        t = make_append(self.w)
+        self.k_new, self.v_new = to_dev(t["k_new"], device), to_dev(t["v_new"], device)
+        shape = (t["num_pages"], self.w.page_size, self.w.Hkv, self.w.d)
+        self.kp = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.vp = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.cu, self.before = i32(t["cu_seqlens_new"], device), i32(t["kv_lens_before"], device)
+        self.pt = i32(t["page_table"], device)
+        self.bytes = 2 * 2 * t["total_new"] * self.w.Hkv * self.w.d * 2
+        self.kind = "append"
+
+    def run(self):
+        import io_aware_exact_flash_gb300 as fa
+
+        fa.fa_paged_append(self.k_new, self.v_new, self.cu, self.before, self.pt, self.kp, self.vp)
+
+    launches = 1
+
+
+class CascadeCase:
+    """Decode batch behind one shared prefix through fa_cascade_fwd (prefix attended once for all
+    query rows, then each suffix, then the merge). Algorithmic bytes: the shared prefix's K/V and
+    every suffix's K/V read once, q read and O, LSE written. The same batch is also timed through
+    fa_paged_fwd with flat page tables (each sequence reading the shared pages itself)."""
+
+    def __init__(self, name, device):
+        import torch
+
+        import io_aware_exact_flash_gb300 as fa
+
+        self.w = w = WORKLOADS[name]
+        t = make_cascade(w)
+        self.q = to_dev(t["q"], device)
+        self.kp, self.vp = to_dev(t["k_pages"], device), to_dev(t["v_pages"], device)
+        self.cu_g, self.pre_t, self.pre_l = (i32(t[k], device) for k in ("cu_q_groups", "prefix_page_table",
+                                                                          "prefix_lens"))
+        self.cu, self.pt, self.kl = (i32(t[k], device) for k in ("cu_seqlens_q", "page_table", "kv_lens"))
+        self.flat_pt, self.flat_kl = i32(t["flat_page_table"], device), i32(t["flat_kv_lens"], device)
+        self.total_q = t["total_q"]
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
+        need = fa.fa_cascade_workspace_bytes(1, w.num_seqs, self.total_q, self.total_q, w.q_len, w.page_size,
+                                             t["prefix_page_table"].shape[1], t["page_table"].shape[1],
+                                             t["num_pages"], w.Hq, w.Hkv, w.d)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        need_flat = fa.fa_paged_workspace_bytes(w.num_seqs, self.total_q, w.q_len, w.page_size,
+                                                t["flat_page_table"].shape[1], t["num_pages"], w.Hq, w.Hkv, w.d)
+        self.ws_flat = torch.empty(max(need_flat, 256), dtype=torch.uint8, device=device)
+        kv_rows = w.prefix_len + int(t["kv_lens"].astype(np.int64).sum())
+        self.bytes = (2 * kv_rows * w.Hkv * w.d * 2 + self.total_q * w.Hq * w.d * 2 * 2 + self.total_q * w.Hq * 4)
+        self.kind = "cascade"
+
+    def run(self):
+        import io_aware_exact_flash_gb300 as fa
+
+        fa.fa_cascade_fwd(self.q, self.kp, self.vp, self.cu_g, self.pre_t, self.pre_l, self.total_q, self.cu,
+                          self.pt, self.kl, self.w.q_len, causal=True, scale=self.w.scale, out=self.o, lse=self.lse,
+                          workspace=self.ws)
+
+    def run_flat(self):
+        import io_aware_exact_flash_gb300 as fa
+
+        fa.fa_paged_fwd(self.q, self.kp, self.vp, self.flat_pt, self.cu, self.flat_kl, self.w.q_len, causal=True,
+                        scale=self.w.scale, out=self.o, lse=self.lse, workspace=self.ws_flat)
+
+    launches = 4  # planning + prefix pass, suffix decode, merge
+
+
+class FlatView:
+    """Times CascadeCase.run_flat with the harness of time_case."""
+
+    def __init__(self, case):
+        self.run = case.run_flat
+
+
+def make_case(name, device):
+    if name.startswith("cascade"):
+        return CascadeCase(name, device)
+    if name.startswith("paged_append"):
+        return AppendCase(name, device)
+    return (PagedCase if name.startswith("paged") else DenseCase)(name, device)
 
 
 def time_case(case, steps, warmup, flush):
@@ -369,11 +465,13 @@ def profile_only(args, device):
         if not hasattr(w, "num_seqs"):
             raise SystemExit("--seqs applies to paged workloads")
         WORKLOADS[args.only] = dataclasses.replace(w, num_seqs=args.seqs)
-    case = (PagedCase if args.only.startswith("paged") else DenseCase)(args.only, device)
+    case = make_case(args.only, device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     ms = statistics.mean(time_case(case, args.steps, args.warmup, flush))
-    if case.kind == "decode":
+    if case.kind in ("decode", "append", "cascade"):
         out = {"workload": args.only, "seqs": case.w.num_seqs, "ms": ms, "GB/s": case.bytes / (ms * 1e-3) / 1e9}
+        if case.kind == "cascade":
+            out["flat_paged_fwd_ms"] = statistics.mean(time_case(FlatView(case), args.steps, args.warmup, flush))
     else:
         out = {"workload": args.only, "ms": ms, "TFLOP/s": case.flops / (ms * 1e-3) / 1e12}
     print(json.dumps(out), flush=True)
@@ -416,7 +514,7 @@ def main(argv=None):
 
     head = DenseCase(HEADLINE, device)
     extra_names = EXTRAS if args.extras == "all" else ([] if args.extras == "none" else args.extras.split(","))
-    extras = [(n, (PagedCase if n.startswith("paged") else DenseCase)(n, device)) for n in extra_names]
+    extras = [(n, make_case(n, device)) for n in extra_names]
 
     sampler = ClockSampler(local)
     barrier(world)
@@ -425,6 +523,7 @@ def main(argv=None):
     t_wall0 = time.perf_counter()
     head_ms = time_case(head, args.steps, args.warmup, flush)
     extra_ms = {n: time_case(c, args.steps, args.warmup, flush) for n, c in extras}
+    flat_ms = {n: time_case(FlatView(c), args.steps, args.warmup, flush) for n, c in extras if c.kind == "cascade"}
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -451,13 +550,18 @@ def main(argv=None):
     extra = {}
     for n, c in extras:
         ms = statistics.mean(extra_ms[n])
-        if c.kind == "decode":
+        if c.kind in ("decode", "append", "cascade"):
             gbs = c.bytes / (ms * 1e-3) / 1e9
-            extra[n] = {"metric": "decode HBM GB/s", "value": gbs, "unit": "GB/s", "ms": ms,
+            extra[n] = {"metric": f"{c.kind} HBM GB/s", "value": gbs, "unit": "GB/s", "ms": ms,
                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                      "frac": gbs / peaks["hbm_gbs"], "peak_source": label,
-                                     "per_launch_bytes": c.bytes},
-                        "splits": c.splits}
+                                     "per_launch_bytes": c.bytes}}
+            if c.kind == "decode":
+                extra[n]["splits"] = c.splits
+            if c.kind == "cascade":
+                fm = statistics.mean(flat_ms[n])
+                extra[n]["flat_paged_fwd_ms"] = fm
+                extra[n]["speedup_vs_flat"] = fm / ms
         else:
             tf = c.flops / (ms * 1e-3) / 1e12
             extra[n] = {"metric": "prefill TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms": ms,
@@ -469,7 +573,8 @@ def main(argv=None):
         v, desc, threads = oracle_sample(head.w, head.host, target_s=12.0)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
 
-    launches = args.steps * (head.launches + sum(c.launches for _, c in extras))
+    launches = args.steps * (head.launches + sum(c.launches for _, c in extras)
+                             + sum(1 for _, c in extras if c.kind == "cascade"))  # the flat comparison
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",

@@ -114,6 +114,68 @@ fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_
                           int H, int d, void* o, float* lse, fa_stream_t stream);
 
 /*
+ * Shared-prefix (cascade) attention over a paged cache.
+ * "I/O-Aware Kernels" (datasystem.school, Module 5), section "FlashInfer: I/O-aware attention
+ * for serving": serving batches reuse long shared prefixes (the prefix sharing of RadixAttention);
+ * keys and values of a prefix that many sequences share are attended once for all of their query
+ * rows, and the result is combined with each sequence's own keys by the LSE merge above.
+ *   Sequences are split into num_groups consecutive groups. Group g owns the query rows
+ *   [cu_q_groups[g], cu_q_groups[g+1]) of q -- the rows of all its sequences, so cu_q_groups[g]
+ *   equals cu_seqlens_q at the group's first sequence; cu_q_groups[0] = 0 and
+ *   cu_q_groups[num_groups] = total_q -- and a shared prefix of prefix_lens[g] keys in the pages
+ *   prefix_page_table[g][0 .. max_prefix_pages).
+ *   Sequence s owns kv_lens[s] further keys (its suffix) in page_table[s][0 .. max_pages_per_seq);
+ *   its query rows [cu_seqlens_q[s], cu_seqlens_q[s+1]) are the last tokens of that suffix.
+ * Result (o bf16 [total_q, Hq, d], lse fp32 [total_q, Hq] or NULL): exactly fa_paged_fwd over the
+ * concatenated keys prefix(g) ++ suffix(s) of every sequence. Every query row sees the whole
+ * prefix; with causal != 0 the suffix is masked bottom-right, which needs q_len(s) <= kv_lens[s]
+ * (the query tokens lie in the suffix). Both passes run the same kernels as fa_paged_fwd (decode
+ * when the pass's max query length is 1, else the tensor-core kernel) with fp32 outputs, then one
+ * merge: three launches plus planning, in order on `stream`.
+ *   max_group_q_len / max_q_len: host-side bounds of the query rows per group / per sequence.
+ *   workspace: at least fa_cascade_workspace_bytes(...) bytes, 256-byte aligned.
+ * Errors as for fa_paged_fwd; also FA_ERR_INVALID_ARG when num_groups > num_seqs.
+ */
+size_t fa_cascade_workspace_bytes(int num_groups, int num_seqs, int total_q, int max_group_q_len,
+                                  int max_q_len, int page_size, int max_prefix_pages,
+                                  int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d);
+fa_status fa_cascade_fwd(const void* q, const void* k_pages, const void* v_pages, int page_size,
+                         int num_pages, int Hq, int Hkv, int d, float scale, int num_groups,
+                         const int32_t* cu_q_groups, const int32_t* prefix_page_table,
+                         const int32_t* prefix_lens, int max_prefix_pages, int max_group_q_len,
+                         int num_seqs, const int32_t* cu_seqlens_q, const int32_t* page_table,
+                         const int32_t* kv_lens, int max_pages_per_seq, int max_q_len, int causal,
+                         int total_q, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                         fa_stream_t stream);
+
+/*
+ * Paged KV append: write the key/value rows of new tokens into their page slots.
+ * "I/O-Aware Kernels" (datasystem.school, Module 5), section "FlashInfer: I/O-aware attention
+ * for serving": the cache is a pool of fixed-size pages reached through a per-sequence page
+ * table; a sequence grows by filling the slot after its current length.
+ *   k_new, v_new:    [total_new, Hkv, d] bf16, the new tokens packed sequence after sequence
+ *                    (may be NULL when total_new == 0);
+ *   cu_seqlens_new:  [num_seqs + 1] int32 (device), row offsets of each sequence's new tokens,
+ *                    cu_seqlens_new[0] == 0 and cu_seqlens_new[num_seqs] == total_new;
+ *   kv_lens_before:  [num_seqs] int32 (device), cached tokens of each sequence before the call;
+ *   page_table:      [num_seqs, max_pages_per_seq] int32 (device), physical page ids;
+ *   k_pages, v_pages: [num_pages, page_size, Hkv, d] bf16, written in place.
+ * New row r of sequence s lands at logical position p = kv_lens_before[s] + r, i.e. in page
+ * page_table[s][p / page_size], slot p % page_size. Nothing else in the pool is touched and
+ * kv_lens_before is not updated (the caller's new length is kv_lens_before + the row count).
+ * The caller must have mapped every page the new rows reach. A row whose position falls outside
+ * the table or whose page id is outside [0, num_pages) is skipped and FA_ERR_DEVICE_BAD_PAGE is
+ * recorded in the device status word. Two rows mapped to one slot race (the caller's error).
+ * Errors: FA_ERR_INVALID_ARG (null pointer, non-positive size), FA_ERR_UNSUPPORTED (d not 64 or
+ * 128; page_size not 16, 32, 64 or 128), FA_ERR_ALIGNMENT (bf16 buffers not 16-byte aligned,
+ * int32 arrays not 4-byte aligned), FA_ERR_CUDA. Asynchronous on `stream`; allocates nothing.
+ */
+fa_status fa_paged_append(const void* k_new, const void* v_new, const int32_t* cu_seqlens_new,
+                          const int32_t* kv_lens_before, const int32_t* page_table, int num_seqs,
+                          int total_new, int page_size, int max_pages_per_seq, int num_pages,
+                          int Hkv, int d, void* k_pages, void* v_pages, fa_stream_t stream);
+
+/*
  * Split-KV paged decode for callers that cannot allocate device memory. The pages have no
  * counterpart of this entry point; it exists for callers that may not call cudaMalloc (for
  * example an engine whose device memory is all handed to a fixed arena, or a plugin inside a

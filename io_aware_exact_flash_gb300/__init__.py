@@ -1,4 +1,5 @@
-"""Exact attention forward for GB300 (sm_103a): dense, paged/ragged prefill and split-KV decode.
+"""Exact attention forward for GB300 (sm_103a): dense, paged/ragged prefill, split-KV decode and
+the paged KV append that feeds them.
 
 The compute path is the C-ABI library ``libfa_gb300.so`` (declared in ``include/fa.h``); this
 package is its thin binding plus the seeded workload generator used by tests and benchmarks.
@@ -6,10 +7,13 @@ package is its thin binding plus the seeded workload generator used by tests and
 from .binding import (  # noqa: F401
     EXPORTED,
     FaError,
+    fa_cascade_fwd,
+    fa_cascade_workspace_bytes,
     fa_decode_num_splits,
     fa_fwd,
     fa_get_device_status,
     fa_merge_states,
+    fa_paged_append,
     fa_paged_decode_noalloc,
     fa_paged_fwd,
     fa_selftest_wait_timeout,

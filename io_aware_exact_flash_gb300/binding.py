@@ -25,7 +25,7 @@ _STATUS_NAMES = {
 
 EXPORTED = ("fa_status_string", "fa_fwd", "fa_paged_fwd", "fa_paged_workspace_bytes",
             "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status", "fa_paged_decode_noalloc",
-            "fa_selftest_wait_timeout")
+            "fa_selftest_wait_timeout", "fa_paged_append", "fa_cascade_fwd", "fa_cascade_workspace_bytes")
 
 
 class FaError(RuntimeError):
@@ -69,6 +69,13 @@ def load_library(path: str = None) -> ctypes.CDLL:
     lib.fa_paged_decode_noalloc.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, ctypes.POINTER(i), ctypes.POINTER(i), vp]
     lib.fa_selftest_wait_timeout.restype = i
+    lib.fa_cascade_workspace_bytes.argtypes = [i] * 12
+    lib.fa_cascade_workspace_bytes.restype = sz
+    lib.fa_cascade_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, i, i, i, vp, vp, vp, i, i, i, i, vp,
+                                   vp, vp, sz, vp]
+    lib.fa_cascade_fwd.restype = i
+    lib.fa_paged_append.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
+    lib.fa_paged_append.restype = i
     lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(i), ctypes.POINTER(i)]
     lib.fa_get_device_status.restype = i
     _lib = lib
@@ -187,6 +194,83 @@ def fa_merge_states(o_parts, lse_parts, out=None, lse=None, return_lse=True, str
                                           _stream(stream))
     _check("fa_merge_states", code)
     return out, lse
+
+
+def fa_cascade_fwd(q, k_pages, v_pages, cu_q_groups, prefix_page_table, prefix_lens, max_group_q_len,
+                   cu_seqlens_q, page_table, kv_lens, max_q_len, causal=True, scale=None, out=None, lse=None,
+                   return_lse=True, workspace=None, stream=None):
+    """Shared-prefix (cascade) attention. Group g of consecutive sequences owns query rows
+    [cu_q_groups[g], cu_q_groups[g+1]) and shares prefix_lens[g] keys in prefix_page_table[g];
+    sequence s adds kv_lens[s] keys of its own in page_table[s]. The result equals fa_paged_fwd over
+    each sequence's prefix ++ suffix keys. Index arrays are int32 CUDA tensors; max_group_q_len and
+    max_q_len are host-side ints. Returns (o, lse)."""
+    _bf16_cuda("q", q, 3)
+    _bf16_cuda("k_pages", k_pages, 4)
+    _bf16_cuda("v_pages", v_pages, 4)
+    for name, t in (("cu_q_groups", cu_q_groups), ("prefix_page_table", prefix_page_table),
+                    ("prefix_lens", prefix_lens), ("cu_seqlens_q", cu_seqlens_q), ("page_table", page_table),
+                    ("kv_lens", kv_lens)):
+        _i32_cuda(name, t)
+    total_q, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_pages.shape
+    num_groups, max_prefix_pages = prefix_page_table.shape
+    num_seqs, max_pages = page_table.shape
+    if dk != d or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]")
+    if cu_q_groups.shape != (num_groups + 1,) or prefix_lens.shape != (num_groups,):
+        raise ValueError("cu_q_groups must be [num_groups + 1] and prefix_lens [num_groups]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    need = lib.fa_cascade_workspace_bytes(num_groups, num_seqs, total_q, int(max_group_q_len), int(max_q_len),
+                                          page_size, max_prefix_pages, max_pages, num_pages, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    code = lib.fa_cascade_fwd(_ptr(q), _ptr(k_pages), _ptr(v_pages), page_size, num_pages, Hq, Hkv, d, scale,
+                              num_groups, _ptr(cu_q_groups), _ptr(prefix_page_table), _ptr(prefix_lens),
+                              max_prefix_pages, int(max_group_q_len), num_seqs, _ptr(cu_seqlens_q), _ptr(page_table),
+                              _ptr(kv_lens), max_pages, int(max_q_len), int(bool(causal)), total_q, _ptr(out),
+                              _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("fa_cascade_fwd", code)
+    return out, lse
+
+
+def fa_cascade_workspace_bytes(num_groups, num_seqs, total_q, max_group_q_len, max_q_len, page_size,
+                               max_prefix_pages, max_pages_per_seq, num_pages, Hq, Hkv, d):
+    return load_library().fa_cascade_workspace_bytes(num_groups, num_seqs, total_q, max_group_q_len, max_q_len,
+                                                     page_size, max_prefix_pages, max_pages_per_seq, num_pages, Hq,
+                                                     Hkv, d)
+
+
+def fa_paged_append(k_new, v_new, cu_seqlens_new, kv_lens_before, page_table, k_pages, v_pages, stream=None):
+    """Write new tokens' K/V rows ([total_new, Hkv, d] bf16) into their page slots, in place.
+
+    New row r of sequence s goes to logical position kv_lens_before[s] + r of that sequence, i.e.
+    page page_table[s][pos // page_size], slot pos % page_size. cu_seqlens_new ([num_seqs + 1]),
+    kv_lens_before ([num_seqs]) and page_table ([num_seqs, max_pages_per_seq]) are int32 CUDA
+    tensors; kv_lens_before is not updated. Returns None."""
+    _bf16_cuda("k_new", k_new, 3)
+    _bf16_cuda("v_new", v_new, 3)
+    _bf16_cuda("k_pages", k_pages, 4)
+    _bf16_cuda("v_pages", v_pages, 4)
+    for name, t in (("cu_seqlens_new", cu_seqlens_new), ("kv_lens_before", kv_lens_before),
+                    ("page_table", page_table)):
+        _i32_cuda(name, t)
+    total_new, Hkv, d = k_new.shape
+    num_pages, page_size, Hkv_p, d_p = k_pages.shape
+    num_seqs, max_pages = page_table.shape
+    if v_new.shape != k_new.shape or v_pages.shape != k_pages.shape or (Hkv_p, d_p) != (Hkv, d):
+        raise ValueError("k_new/v_new must be [total_new, Hkv, d] and the pages [num_pages, page_size, Hkv, d]")
+    if cu_seqlens_new.shape != (num_seqs + 1,) or kv_lens_before.shape != (num_seqs,):
+        raise ValueError("cu_seqlens_new must be [num_seqs + 1] and kv_lens_before [num_seqs]")
+    code = load_library().fa_paged_append(_ptr(k_new), _ptr(v_new), _ptr(cu_seqlens_new), _ptr(kv_lens_before),
+                                          _ptr(page_table), num_seqs, total_new, page_size, max_pages, num_pages,
+                                          Hkv, d, _ptr(k_pages), _ptr(v_pages), _stream(stream))
+    _check("fa_paged_append", code)
 
 
 def fa_get_device_status(stream=None):

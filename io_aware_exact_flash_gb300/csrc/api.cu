@@ -185,6 +185,128 @@ int fa::current_device_info(DeviceStatus** status, int* sm_count) {
   return FA_OK;
 }
 
+namespace {
+
+// Shape checks shared by fa_paged_fwd and the two passes of fa_cascade_fwd.
+fa_status check_paged_shape(int num_seqs, int total_q, int max_q_len, int page_size, int max_pages_per_seq,
+                            int num_pages, int Hq, int Hkv, int d, int num_splits, float scale) {
+  if (num_seqs <= 0 || total_q < 0 || max_q_len < 1 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0 ||
+      Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0 || !scale_ok(scale))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)max_pages_per_seq * page_size > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31) - 1)
+    return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Workspace of one paged pass (decode partials, or the prefill work list).
+size_t paged_pass_workspace(int num_seqs, int total_q, int max_q_len, int page_size, int max_pages_per_seq,
+                            int num_pages, int Hq, int Hkv, int d, int num_splits, int sm_count) {
+  if (max_q_len == 1) {
+    const DecodePlan dp = plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, sm_count);
+    return decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);
+  }
+  return prefill_workspace(num_seqs, total_q);
+}
+
+// Enqueue one validated paged pass. O goes to `o` as bf16, or to `o_f32` as fp32 when that is set.
+fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* page_table, const int32_t* cu_seqlens_q, const int32_t* kv_lens, int num_seqs,
+                        int total_q, int max_q_len, int page_size, int max_pages_per_seq, int num_pages, int Hq,
+                        int Hkv, int d, int causal, float scale, void* o, float* o_f32, float* lse, void* workspace,
+                        size_t workspace_bytes, int num_splits, fa_stream_t stream) {
+  if (total_q == 0) return FA_OK;
+  const int group = Hq / Hkv;
+
+  if (max_q_len == 1) {
+    // ------------------------------------------------------------- split-KV decode
+    if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
+    const DecodePlan dp =
+        plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, dev->sm_count);
+    const size_t need = decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_ALIGNMENT;
+    fa::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.k_pages = k_pages;
+    p.v_pages = v_pages;
+    p.page_table = page_table;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.kv_lens = kv_lens;
+    p.o = o;
+    p.o_f32 = o_f32;
+    p.lse = lse;
+    if (need > 0) fa::decode_scratch_layout(workspace, dp.splits, num_seqs, Hq, d, p);
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = group;
+    p.page_size = page_size;
+    p.max_pages_per_seq = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.pages_per_split = dp.pages_per_split;
+    p.num_splits = dp.splits;
+    p.heads_per_cta = dp.heads_per_cta;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.status = dev->status;
+    return fa::launch_decode(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  // --------------------------------------------------------------- tensor-core prefill
+  const size_t need = prefill_workspace(num_seqs, total_q);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+  fa::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
+    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)fa::kBM, 1};
+    if (!make_map(&p.tm_q, q, dims, str, box)) return FA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)num_pages};
+    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2, (uint64_t)page_size * Hkv * d * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)page_size, 1};
+    if (!make_map(&p.tm_k, k_pages, dims, str, box) || !make_map(&p.tm_v, v_pages, dims, str, box))
+      return FA_ERR_CUDA;
+  }
+  int* work_count = static_cast<int*>(workspace);
+  int2* work_list = reinterpret_cast<int2*>(static_cast<char*>(workspace) + 256);
+  p.o = o;
+  p.o_f32 = o_f32;
+  p.lse = lse;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = group;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.page_table = page_table;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.kv_lens = kv_lens;
+  p.page_size = page_size;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.work_list = work_list;
+  p.work_count = work_count;
+  p.status = dev->status;
+  long long max_kv_tiles = ((long long)max_pages_per_seq * page_size + fa::kBN - 1) / fa::kBN;
+  if (max_kv_tiles > 8192) max_kv_tiles = 8192;  // cost buckets only order the work
+  return fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q), (int)max_kv_tiles,
+                                  work_list, work_count, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {
@@ -257,12 +379,8 @@ size_t fa_paged_workspace_bytes(int num_seqs, int total_q, int max_q_len, int pa
                                 int num_pages, int Hq, int Hkv, int d, int num_splits) {
   if (num_seqs <= 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0)
     return 0;
-  if (max_q_len == 1) {
-    const DecodePlan dp =
-        plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, sm_count_now());
-    return decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);
-  }
-  return prefill_workspace(num_seqs, total_q);
+  return paged_pass_workspace(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d,
+                              num_splits, sm_count_now());
 }
 
 fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
@@ -271,103 +389,93 @@ fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, 
                        float scale, void* o, float* lse, void* workspace, size_t workspace_bytes, int num_splits,
                        fa_stream_t stream) {
   if (!q || !k_pages || !v_pages || !page_table || !cu_seqlens_q || !kv_lens || !o) return FA_ERR_INVALID_ARG;
-  if (num_seqs <= 0 || total_q < 0 || max_q_len < 1 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0 ||
-      Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0 || !scale_ok(scale))
-    return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FA_ERR_UNSUPPORTED;
-  if ((long long)max_pages_per_seq * page_size > (1LL << 30) || (long long)num_pages * page_size > (1LL << 31) - 1)
-    return FA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
-      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+  fa_status err = check_paged_shape(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d,
+                                    num_splits, scale);
+  if (err != FA_OK) return err;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || (lse && !aligned4(lse)) ||
+      !aligned4(page_table) || !aligned4(cu_seqlens_q) || !aligned4(kv_lens))
     return FA_ERR_ALIGNMENT;
-  fa_status err = FA_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+  return enqueue_paged(dev, q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, num_seqs, total_q, max_q_len,
+                       page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, causal, scale, o, nullptr, lse, workspace,
+                       workspace_bytes, num_splits, stream);
+}
+
+// Shared-prefix (cascade) attention: the prefix pass and the suffix pass each leave an fp32 partial
+// state (O normalised over its own keys, natural-log LSE) in the workspace; the merge combines them.
+// Workspace: O parts [2, total_q, Hq, d] fp32 | LSE parts [2, total_q, Hq] fp32 | the passes' own
+// scratch (reused by both, which run one after the other on the stream).
+namespace {
+size_t cascade_parts_bytes(int total_q, int Hq, int d, size_t* lse_offset) {
+  const size_t o_bytes = align_up((size_t)2 * total_q * Hq * d * sizeof(float), 256);
+  if (lse_offset) *lse_offset = o_bytes;
+  return o_bytes + align_up((size_t)2 * total_q * Hq * sizeof(float), 256);
+}
+}  // namespace
+
+size_t fa_cascade_workspace_bytes(int num_groups, int num_seqs, int total_q, int max_group_q_len, int max_q_len,
+                                  int page_size, int max_prefix_pages, int max_pages_per_seq, int num_pages, int Hq,
+                                  int Hkv, int d) {
+  if (check_paged_shape(num_groups, total_q, max_group_q_len, page_size, max_prefix_pages, num_pages, Hq, Hkv, d, 0,
+                        1.f) != FA_OK ||
+      check_paged_shape(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, 0, 1.f) !=
+          FA_OK)
+    return 0;
+  const int sms = sm_count_now();
+  const size_t a = paged_pass_workspace(num_groups, total_q, max_group_q_len, page_size, max_prefix_pages, num_pages,
+                                        Hq, Hkv, d, 0, sms);
+  const size_t b =
+      paged_pass_workspace(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, 0, sms);
+  return cascade_parts_bytes(total_q, Hq, d, nullptr) + (a > b ? a : b);
+}
+
+fa_status fa_cascade_fwd(const void* q, const void* k_pages, const void* v_pages, int page_size, int num_pages, int Hq,
+                         int Hkv, int d, float scale, int num_groups, const int32_t* cu_q_groups,
+                         const int32_t* prefix_page_table, const int32_t* prefix_lens, int max_prefix_pages,
+                         int max_group_q_len, int num_seqs, const int32_t* cu_seqlens_q, const int32_t* page_table,
+                         const int32_t* kv_lens, int max_pages_per_seq, int max_q_len, int causal, int total_q, void* o,
+                         float* lse, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !cu_q_groups || !prefix_page_table || !prefix_lens || !cu_seqlens_q ||
+      !page_table || !kv_lens || !o)
+    return FA_ERR_INVALID_ARG;
+  fa_status err = check_paged_shape(num_groups, total_q, max_group_q_len, page_size, max_prefix_pages, num_pages, Hq,
+                                    Hkv, d, 0, scale);
+  if (err != FA_OK) return err;
+  err = check_paged_shape(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, 0, scale);
+  if (err != FA_OK) return err;
+  if (num_groups > num_seqs) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || (lse && !aligned4(lse)) ||
+      !aligned4(cu_q_groups) || !aligned4(prefix_page_table) || !aligned4(prefix_lens) || !aligned4(cu_seqlens_q) ||
+      !aligned4(page_table) || !aligned4(kv_lens))
+    return FA_ERR_ALIGNMENT;
   const DeviceInfo* dev = current_device(&err);
   if (!dev) return err;
   if (total_q == 0) return FA_OK;
-  const int group = Hq / Hkv;
-
-  if (max_q_len == 1) {
-    // ------------------------------------------------------------- split-KV decode
-    if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
-    const DecodePlan dp =
-        plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, dev->sm_count);
-    const size_t need = decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);
-    if (need > 0 && (!workspace || workspace_bytes < need)) return FA_ERR_WORKSPACE;
-    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_ALIGNMENT;
-    fa::DecodeParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.q = q;
-    p.k_pages = k_pages;
-    p.v_pages = v_pages;
-    p.page_table = page_table;
-    p.cu_seqlens_q = cu_seqlens_q;
-    p.kv_lens = kv_lens;
-    p.o = o;
-    p.lse = lse;
-    if (need > 0) fa::decode_scratch_layout(workspace, dp.splits, num_seqs, Hq, d, p);
-    p.num_seqs = num_seqs;
-    p.total_q = total_q;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.group = group;
-    p.page_size = page_size;
-    p.max_pages_per_seq = max_pages_per_seq;
-    p.num_pages = num_pages;
-    p.pages_per_split = dp.pages_per_split;
-    p.num_splits = dp.splits;
-    p.heads_per_cta = dp.heads_per_cta;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    p.status = dev->status;
-    return fa::launch_decode(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-  }
-
-  // --------------------------------------------------------------- tensor-core prefill
-  const size_t need = prefill_workspace(num_seqs, total_q);
+  const size_t need = fa_cascade_workspace_bytes(num_groups, num_seqs, total_q, max_group_q_len, max_q_len, page_size,
+                                                 max_prefix_pages, max_pages_per_seq, num_pages, Hq, Hkv, d);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
-  fa::PrefillParams p;
-  std::memset(&p, 0, sizeof(p));
-  {
-    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
-    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
-    const uint32_t box[4] = {64, 1, (uint32_t)fa::kBM, 1};
-    if (!make_map(&p.tm_q, q, dims, str, box)) return FA_ERR_CUDA;
-  }
-  {
-    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)num_pages};
-    const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2, (uint64_t)page_size * Hkv * d * 2};
-    const uint32_t box[4] = {64, 1, (uint32_t)page_size, 1};
-    if (!make_map(&p.tm_k, k_pages, dims, str, box) || !make_map(&p.tm_v, v_pages, dims, str, box))
-      return FA_ERR_CUDA;
-  }
-  int* work_count = static_cast<int*>(workspace);
-  int2* work_list = reinterpret_cast<int2*>(static_cast<char*>(workspace) + 256);
-  p.o = o;
-  p.lse = lse;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.group = group;
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  p.page_table = page_table;
-  p.cu_seqlens_q = cu_seqlens_q;
-  p.kv_lens = kv_lens;
-  p.page_size = page_size;
-  p.max_pages_per_seq = max_pages_per_seq;
-  p.num_pages = num_pages;
-  p.num_seqs = num_seqs;
-  p.total_q = total_q;
-  p.work_list = work_list;
-  p.work_count = work_count;
-  p.status = dev->status;
-  long long max_kv_tiles = ((long long)max_pages_per_seq * page_size + fa::kBN - 1) / fa::kBN;
-  if (max_kv_tiles > 8192) max_kv_tiles = 8192;  // cost buckets only order the work
-  return fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q), (int)max_kv_tiles,
-                                  work_list, work_count, stream) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_CUDA;
+  size_t lse_off = 0;
+  const size_t parts = cascade_parts_bytes(total_q, Hq, d, &lse_off);
+  char* base = static_cast<char*>(workspace);
+  float* o_parts = reinterpret_cast<float*>(base);
+  float* lse_parts = reinterpret_cast<float*>(base + lse_off);
+  const size_t part_rows = (size_t)total_q * Hq;
+  void* scratch = base + parts;
+  const size_t scratch_bytes = workspace_bytes - parts;
+  // prefix pass: every query row of a group sees all of the group's shared keys
+  err = enqueue_paged(dev, q, k_pages, v_pages, prefix_page_table, cu_q_groups, prefix_lens, num_groups, total_q,
+                      max_group_q_len, page_size, max_prefix_pages, num_pages, Hq, Hkv, d, 0, scale, nullptr, o_parts,
+                      lse_parts, scratch, scratch_bytes, 0, stream);
+  if (err != FA_OK) return err;
+  // suffix pass: each sequence's own keys, with the caller's masking
+  err = enqueue_paged(dev, q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, num_seqs, total_q, max_q_len,
+                      page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, causal, scale, nullptr,
+                      o_parts + part_rows * d, lse_parts + part_rows, scratch, scratch_bytes, 0, stream);
+  if (err != FA_OK) return err;
+  return fa::launch_merge(o_parts, lse_parts, 2, total_q, Hq, d, o, lse, false, stream) == cudaSuccess ? FA_OK
+                                                                                                      : FA_ERR_CUDA;
 }
 
 fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_parts, int n_rows, int H, int d,

@@ -250,7 +250,17 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
       const int h = hk * G + g;
       const float inv_l = l[g] > 0.f ? 1.f / l[g] : 0.f;
       const float lse2 = l[g] > 0.f ? m[g] + __log2f(l[g]) : -INFINITY;
-      if (p.num_splits == 1) {
+      if (p.num_splits == 1 && p.o_f32 != nullptr) {
+        float4* op = reinterpret_cast<float4*>(p.o_f32 + ((int64_t)tok * p.Hq + h) * D);
+#pragma unroll
+        for (int c = 0; c < C::CPL; ++c) {
+          op[2 * (lr + c * C::LPR)] = make_float4(o[g][c * 8 + 0] * inv_l, o[g][c * 8 + 1] * inv_l,
+                                                  o[g][c * 8 + 2] * inv_l, o[g][c * 8 + 3] * inv_l);
+          op[2 * (lr + c * C::LPR) + 1] = make_float4(o[g][c * 8 + 4] * inv_l, o[g][c * 8 + 5] * inv_l,
+                                                      o[g][c * 8 + 6] * inv_l, o[g][c * 8 + 7] * inv_l);
+        }
+        if (lr == 0 && p.lse) p.lse[(int64_t)tok * p.Hq + h] = lse2 * kLn2;
+      } else if (p.num_splits == 1) {
         __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.o) + ((int64_t)tok * p.Hq + h) * D;
 #pragma unroll
         for (int c = 0; c < C::CPL; ++c) {
@@ -317,10 +327,15 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
       }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2 packed;
-    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.o) + ((int64_t)tok * p.Hq + h) * D)[e4] = packed;
+    if (p.o_f32 != nullptr) {
+      reinterpret_cast<float4*>(p.o_f32 + ((int64_t)tok * p.Hq + h) * D)[e4] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.o) + ((int64_t)tok * p.Hq + h) * D)[e4] = packed;
+    }
     if (e4 == 0 && p.lse != nullptr) p.lse[(int64_t)tok * p.Hq + h] = wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
   }
 }

@@ -24,7 +24,8 @@ struct alignas(64) PrefillParams {
   CUtensorMap tm_q;  // dense: (d, Hq, S, B)        paged: (d, Hq, total_q, 1)
   CUtensorMap tm_k;  // dense: (d, Hkv, S, B)       paged: (d, Hkv, page_size, num_pages)
   CUtensorMap tm_v;
-  void* o;           // bf16 output
+  void* o;           // bf16 output (unused when o_f32 is set)
+  float* o_f32;      // fp32 output instead of bf16 (a partial state for an LSE merge) or null
   float* lse;        // fp32 output or null
   int Hq, Hkv, group;
   int causal;
@@ -51,7 +52,8 @@ struct DecodeParams {
   const int32_t* page_table;
   const int32_t* cu_seqlens_q;
   const int32_t* kv_lens;
-  void* o;                 // bf16 [total_q, Hq, d] (used when num_splits == 1)
+  void* o;                 // bf16 [total_q, Hq, d] (unused when o_f32 is set)
+  float* o_f32;            // fp32 [total_q, Hq, d] instead of bf16, or null
   float* lse;              // fp32 [total_q, Hq] or null
   float* o_part;           // fp32 [num_splits, num_seqs, Hq, d]
   float* lse_part;         // fp32 [num_splits, num_seqs, Hq]  (log2 domain, scaled)

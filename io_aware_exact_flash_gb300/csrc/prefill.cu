@@ -579,7 +579,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const int64_t tok = w.tok0 + row;
       const bool store = row < w.q_len && (!PAGED || tok < p.total_q);
-      if (store) {
+      if (store && p.o_f32 != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(p.o_f32 + (tok * p.Hq + w.h) * D);
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i)
+          dst[i] = make_float4(u2f(orr[4 * i + 0]) * inv_l, u2f(orr[4 * i + 1]) * inv_l,
+                               u2f(orr[4 * i + 2]) * inv_l, u2f(orr[4 * i + 3]) * inv_l);
+      } else if (store) {
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + w.h) * D);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i)
@@ -587,8 +593,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                               pack_bf16x2(u2f(orr[8 * i + 2]) * inv_l, u2f(orr[8 * i + 3]) * inv_l),
                               pack_bf16x2(u2f(orr[8 * i + 4]) * inv_l, u2f(orr[8 * i + 5]) * inv_l),
                               pack_bf16x2(u2f(orr[8 * i + 6]) * inv_l, u2f(orr[8 * i + 7]) * inv_l));
-        if (p.lse != nullptr) p.lse[tok * p.Hq + w.h] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
       }
+      if (store && p.lse != nullptr)
+        p.lse[tok * p.Hq + w.h] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
       __syncwarp();
     }
   }

@@ -179,6 +179,76 @@ def make_paged(w: PagedWorkload):
     return lay
 
 
+def make_append(w: PagedWorkload):
+    """A cache fill: every key/value row of the batch's sequences, packed sequence after sequence,
+    to be appended into an empty pool (kv_lens_before = 0). Returns the layout plus k_new, v_new
+    (uint16 bf16 bits, [total_new, Hkv, d]), cu_seqlens_new and kv_lens_before."""
+    lay = paged_layout(w)
+    total = int(lay["kv_lens"].astype(np.int64).sum())
+    cu = np.zeros(len(lay["kv_lens"]) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lay["kv_lens"])
+    lay.update(k_new=normal_bf16(w.seed, (total, w.Hkv, w.d), 1.0, stream=30),
+               v_new=normal_bf16(w.seed, (total, w.Hkv, w.d), 1.0, stream=31),
+               cu_seqlens_new=cu, kv_lens_before=np.zeros(len(lay["kv_lens"]), dtype=np.int32), total_new=total)
+    return lay
+
+
+@dataclass
+class CascadeWorkload:
+    """A decode-style batch whose sequences share one prefix: num_seqs sequences, each with q_len
+    query tokens at the end of its own suffix (suffix lengths uniform in [suffix_lo, suffix_hi]),
+    all behind the same prefix_len shared keys. One pool holds the prefix pages once and every
+    sequence's suffix pages."""
+
+    name: str
+    num_seqs: int
+    prefix_len: int
+    suffix_lo: int
+    suffix_hi: int
+    q_len: int
+    Hq: int
+    Hkv: int
+    d: int
+    page_size: int
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+def make_cascade(w: CascadeWorkload):
+    """Cascade inputs plus the same batch laid out flat (each sequence's table lists the shared
+    prefix pages, then its own; valid when prefix_len is a multiple of page_size)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 7])))
+    kv_lens = g.integers(w.suffix_lo, w.suffix_hi + 1, size=w.num_seqs).astype(np.int32)
+    ps = w.page_size
+    n_prefix = (w.prefix_len + ps - 1) // ps
+    n_suffix = (kv_lens + ps - 1) // ps
+    P = int(n_prefix + n_suffix.sum())
+    perm = g.permutation(P).astype(np.int32)
+    prefix_table = perm[:n_prefix].reshape(1, -1).copy() if n_prefix else np.full((1, 1), -1, np.int32)
+    table = np.full((w.num_seqs, max(1, int(n_suffix.max()))), -1, dtype=np.int32)
+    off = n_prefix
+    for s, n in enumerate(n_suffix):
+        table[s, :n] = perm[off:off + n]
+        off += n
+    q_lens = np.full(w.num_seqs, w.q_len, dtype=np.int32)
+    cu = np.zeros(w.num_seqs + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    total_q = int(cu[-1])
+    flat = np.full((w.num_seqs, n_prefix + table.shape[1]), -1, dtype=np.int32)
+    flat[:, :n_prefix] = prefix_table[0, :n_prefix]
+    flat[:, n_prefix:] = table
+    return dict(
+        q=normal_bf16(w.seed, (total_q, w.Hq, w.d), 1.0, stream=10),
+        k_pages=normal_bf16(w.seed, (P, ps, w.Hkv, w.d), 1.0, stream=11),
+        v_pages=normal_bf16(w.seed, (P, ps, w.Hkv, w.d), 1.0, stream=12),
+        num_pages=P, cu_q_groups=np.array([0, total_q], dtype=np.int32), prefix_page_table=prefix_table,
+        prefix_lens=np.array([w.prefix_len], dtype=np.int32), cu_seqlens_q=cu, q_lens=q_lens, page_table=table,
+        kv_lens=kv_lens, total_q=total_q, flat_page_table=flat, flat_kv_lens=(kv_lens + w.prefix_len).astype(np.int32))
+
+
 def paged_allowed_scores(lay, Hq: int, causal: bool) -> int:
     total = 0
     for ql, kl in zip(lay["q_lens"].tolist(), lay["kv_lens"].tolist()):
@@ -208,4 +278,12 @@ WORKLOADS = {
     "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16": PagedWorkload(
         "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16", num_seqs=128, len_lo=1024,
         len_hi=16384, Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=True, seed=1004),
+    # 128 decode sequences behind one shared 16384-token prefix, own suffixes of 256..2048 tokens
+    "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16": CascadeWorkload(
+        "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16", num_seqs=128, prefix_len=16384,
+        suffix_lo=256, suffix_hi=2048, q_len=1, Hq=32, Hkv=8, d=128, page_size=16, seed=1005),
+    # the K/V cache fill of the paged prefill batch above (same lengths and page table)
+    "paged_append_64seq_512_8192_hkv8_d128_p16": PagedWorkload(
+        "paged_append_64seq_512_8192_hkv8_d128_p16", num_seqs=64, len_lo=512, len_hi=8192,
+        Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=False, seed=1003),
 }

@@ -110,3 +110,29 @@ def test_merge_host_validation(lib):
     assert lib.fa_merge_states(vp(FAKE), vp(FAKE), 0, 4, 8, 128, vp(FAKE), None, None) == 1
     assert lib.fa_merge_states(vp(FAKE), vp(FAKE), 2, 4, 8, 100, vp(FAKE), None, None) == 2
     assert lib.fa_merge_states(vp(FAKE + 4), vp(FAKE), 2, 4, 8, 128, vp(FAKE), None, None) == 3
+
+
+def _append(lib, **kw):
+    a = dict(kn=FAKE, vn=FAKE, cu=FAKE, kl=FAKE, pt=FAKE, num_seqs=2, total_new=10, ps=16, max_pages=4,
+             num_pages=8, Hkv=2, d=128, kp=FAKE, vp_=FAKE)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.fa_paged_append(vp(a["kn"]), vp(a["vn"]), vp(a["cu"]), vp(a["kl"]), vp(a["pt"]), a["num_seqs"],
+                               a["total_new"], a["ps"], a["max_pages"], a["num_pages"], a["Hkv"], a["d"],
+                               vp(a["kp"]), vp(a["vp_"]), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kn=0), 1), (dict(pt=0), 1), (dict(vp_=0), 1), (dict(num_seqs=0), 1), (dict(total_new=-1), 1),
+    (dict(num_pages=0), 1), (dict(Hkv=0), 1), (dict(max_pages=0), 1),
+    (dict(d=96), 2), (dict(ps=24), 2), (dict(ps=256), 2),
+    (dict(kn=FAKE + 8), 3), (dict(kp=FAKE + 4), 3), (dict(cu=FAKE + 2), 3), (dict(kl=FAKE + 1), 3),
+])
+def test_fa_paged_append_host_validation(lib, kw, code):
+    assert _append(lib, **kw) == code
+
+
+def test_fa_paged_append_empty_rows_may_be_null(lib):
+    # nothing to append: NULL row buffers pass validation (the call then needs a device)
+    assert _append(lib, kn=0, vn=0, total_new=0) != 1
+    assert _append(lib, kn=0, total_new=1) == 1
