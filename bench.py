@@ -4,8 +4,9 @@ One timed step is one forward pass of causal prefill attention over the workload
 metric is quoted on (B=4, Hq=Hkv=32, S=4096, d=128, bf16, synthetic N(0,1) inputs). The same run
 also times, with the same step and warm-up counts, the other workloads of the hot path: long-context
 GQA prefill (S=32768), paged ragged prefill (64 sequences), paged split-KV decode (128
-sequences) and the paged KV append that fills the prefill batch's cache; their numbers go to the
-"extra" object of the single JSON line rank 0 prints.
+sequences), the paged KV append that fills the prefill batch's cache, decode behind a shared
+prefix (cascade), a batch mixing prefill, chunked prefill and decode, and multi-token verify;
+their numbers go to the "extra" object of the single JSON line rank 0 prints.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -34,6 +35,8 @@ if ROOT not in sys.path:
 
 from io_aware_exact_flash_gb300.workloads import (  # noqa: E402
     WORKLOADS,
+    CascadeWorkload,
+    PagedWorkload,
     make_append,
     make_cascade,
     make_dense,
@@ -45,7 +48,8 @@ METRIC = "attn fwd TFLOP/s (prefill) & decode HBM GB/s on 1 GB300, % of roofline
 HEADLINE = "causal_prefill_b4_h32_s4096_d128"
 EXTRAS = ["gqa_causal_prefill_b1_hq32_hkv8_s32768_d128", "paged_prefill_64seq_512_8192_hq32_hkv8_d128_p16",
           "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16", "paged_append_64seq_512_8192_hkv8_d128_p16",
-          "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16"]
+          "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16",
+          "mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16", "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) of one headline prefill launch from the ncu capture summarised in
 # profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on; the
@@ -227,16 +231,17 @@ class PagedCase:
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.scores = paged_allowed_scores(t, self.w.Hq, self.w.causal)
         self.flops = 4.0 * self.w.d * self.scores
-        self.kind = "decode" if self.w.decode else "prefill"
+        # verify batches (a few query rows per sequence) are bound by reading K/V, like decode
+        self.kind = "decode" if self.w.decode else ("verify" if 0 < self.w.q_hi <= 16 else "prefill")
         # algorithmic bytes of decode: every K and V row read once, q read, o and lse written
         kv_rows = int(t["kv_lens"].astype(np.int64).sum())
         self.bytes = (2 * kv_rows * self.w.Hkv * self.w.d * 2 + t["total_q"] * self.w.Hq * self.w.d * 2 * 2
                       + t["total_q"] * self.w.Hq * 4)
-        if self.w.decode:
-            self.splits = fa.fa_decode_num_splits(self.w.num_seqs, self.w.page_size, t["page_table"].shape[1],
-                                                  t["num_pages"], self.w.Hkv)
-        else:
-            self.splits = 1
+        self.splits = fa.fa_paged_num_splits(self.w.num_seqs, t["total_q"], self.max_q, self.w.page_size,
+                                             t["page_table"].shape[1], t["num_pages"], self.w.Hq, self.w.Hkv,
+                                             self.w.d)
+        g = self.w.Hq // self.w.Hkv
+        self.tensor_cores = not (self.w.decode and g not in (2, 4, 8))
 
     def run(self):
         import io_aware_exact_flash_gb300 as fa
@@ -246,9 +251,12 @@ class PagedCase:
 
     @property
     def launches(self):
-        # prefill: the planning kernel and the attention kernel; decode: one kernel (the merge is
-        # fused into it; its counter reset is a cudaMemsetAsync, not a kernel)
-        return 1 if self.w.decode else 2
+        # tensor-core path: the planning kernel, the attention kernel, and the merge when the keys
+        # are split; CUDA-core decode: one kernel (its merge is fused; the counter reset is a
+        # cudaMemsetAsync, not a kernel)
+        if not self.tensor_cores:
+            return 1
+        return 2 + (self.splits > 1)
 
 
 class AppendCase:
@@ -306,6 +314,14 @@ class CascadeCase:
         need_flat = fa.fa_paged_workspace_bytes(w.num_seqs, self.total_q, w.q_len, w.page_size,
                                                 t["flat_page_table"].shape[1], t["num_pages"], w.Hq, w.Hkv, w.d)
         self.ws_flat = torch.empty(max(need_flat, 256), dtype=torch.uint8, device=device)
+        # launches: each pass is planning + attention (+ a merge when its keys are split), then the
+        # merge of the two passes
+        sp_pre = fa.fa_paged_num_splits(1, self.total_q, self.total_q, w.page_size, t["prefix_page_table"].shape[1],
+                                        t["num_pages"], w.Hq, w.Hkv, w.d)
+        sp_suf = fa.fa_paged_num_splits(w.num_seqs, self.total_q, w.q_len, w.page_size, t["page_table"].shape[1],
+                                        t["num_pages"], w.Hq, w.Hkv, w.d)
+        self.launches = (2 + (sp_pre > 1)) + (2 + (sp_suf > 1)) + 1
+        self.prefix_splits = sp_pre
         kv_rows = w.prefix_len + int(t["kv_lens"].astype(np.int64).sum())
         self.bytes = (2 * kv_rows * w.Hkv * w.d * 2 + self.total_q * w.Hq * w.d * 2 * 2 + self.total_q * w.Hq * 4)
         self.kind = "cascade"
@@ -323,7 +339,6 @@ class CascadeCase:
         fa.fa_paged_fwd(self.q, self.kp, self.vp, self.flat_pt, self.cu, self.flat_kl, self.w.q_len, causal=True,
                         scale=self.w.scale, out=self.o, lse=self.lse, workspace=self.ws_flat)
 
-    launches = 4  # planning + prefix pass, suffix decode, merge
 
 
 class FlatView:
@@ -334,11 +349,12 @@ class FlatView:
 
 
 def make_case(name, device):
-    if name.startswith("cascade"):
+    w = WORKLOADS[name]
+    if isinstance(w, CascadeWorkload):
         return CascadeCase(name, device)
     if name.startswith("paged_append"):
         return AppendCase(name, device)
-    return (PagedCase if name.startswith("paged") else DenseCase)(name, device)
+    return (PagedCase if isinstance(w, PagedWorkload) else DenseCase)(name, device)
 
 
 def time_case(case, steps, warmup, flush):
@@ -468,7 +484,7 @@ def profile_only(args, device):
     case = make_case(args.only, device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     ms = statistics.mean(time_case(case, args.steps, args.warmup, flush))
-    if case.kind in ("decode", "append", "cascade"):
+    if case.kind in ("decode", "append", "cascade", "verify"):
         out = {"workload": args.only, "seqs": case.w.num_seqs, "ms": ms, "GB/s": case.bytes / (ms * 1e-3) / 1e9}
         if case.kind == "cascade":
             out["flat_paged_fwd_ms"] = statistics.mean(time_case(FlatView(case), args.steps, args.warmup, flush))
@@ -550,14 +566,17 @@ def main(argv=None):
     extra = {}
     for n, c in extras:
         ms = statistics.mean(extra_ms[n])
-        if c.kind in ("decode", "append", "cascade"):
+        if c.kind in ("decode", "append", "cascade", "verify"):
             gbs = c.bytes / (ms * 1e-3) / 1e9
             extra[n] = {"metric": f"{c.kind} HBM GB/s", "value": gbs, "unit": "GB/s", "ms": ms,
                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                      "frac": gbs / peaks["hbm_gbs"], "peak_source": label,
                                      "per_launch_bytes": c.bytes}}
-            if c.kind == "decode":
+            if isinstance(c, PagedCase):
                 extra[n]["splits"] = c.splits
+                extra[n]["path"] = "tensor cores" if c.tensor_cores else "cuda cores"
+            if c.kind == "verify":
+                extra[n]["tflops"] = c.flops / (ms * 1e-3) / 1e12
             if c.kind == "cascade":
                 fm = statistics.mean(flat_ms[n])
                 extra[n]["flat_paged_fwd_ms"] = fm
@@ -574,7 +593,7 @@ def main(argv=None):
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
 
     launches = args.steps * (head.launches + sum(c.launches for _, c in extras)
-                             + sum(1 for _, c in extras if c.kind == "cascade"))  # the flat comparison
+                             + sum(2 for _, c in extras if c.kind == "cascade"))  # the flat comparison
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",

@@ -76,11 +76,14 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  *                  cu[num_seqs] = total_q);
  *   kv_lens:       [num_seqs] int32 key/value lengths, 0 <= kv_len <= max_pages_per_seq*page_size;
  *   lse:           [total_q, Hq] fp32 or NULL.
- *   max_q_len:     the largest query length (a host-side bound, used for planning). When it is 1
- *                  the batch is decoded with split-KV (each sequence's keys are split into
- *                  num_splits chunks, attended in parallel, and merged by their LSE);
- *                  otherwise the tiled tensor-core prefill kernel runs.
- *   num_splits:    split count for decode; 0 chooses one from the SM count.
+ *   max_q_len:     the largest query length (a host-side bound, used for planning).
+ *                  Batches run on the tiled tensor-core kernel; with a GQA group (Hq / Hkv) of
+ *                  2, 4 or 8 the group's query heads share each tile (rows = token x head), so
+ *                  decode and multi-token verify rows fill the tensor core too. A decode batch
+ *                  (max_q_len == 1) with any other group runs on a split-KV CUDA-core kernel.
+ *   num_splits:    key splits: each sequence's keys are cut into num_splits contiguous ranges,
+ *                  attended in parallel as fp32 partial states and merged by their LSE. 0 chooses
+ *                  from the SM count (splits only when there is too little other parallelism).
  *   workspace:     device scratch of at least fa_paged_workspace_bytes(...) bytes (may be NULL
  *                  when that function returns 0). Its contents need no initialisation; calls that
  *                  share a workspace must be ordered on one stream.
@@ -98,7 +101,13 @@ size_t fa_paged_workspace_bytes(int num_seqs, int total_q, int max_q_len, int pa
                                 int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d,
                                 int num_splits);
 
-/* The split count fa_paged_fwd uses for a decode batch with these sizes (num_splits = 0). */
+/* The key-split count fa_paged_fwd plans for a batch with these sizes (num_splits = 0): 1 means
+ * no split. Host-side only. */
+int fa_paged_num_splits(int num_seqs, int total_q, int max_q_len, int page_size,
+                        int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d);
+
+/* The split count the split-KV CUDA-core decode kernel uses for a decode batch with these sizes
+ * (num_splits = 0): the path of decode batches whose GQA group is not 2, 4 or 8. */
 int fa_decode_num_splits(int num_seqs, int page_size, int max_pages_per_seq, int num_pages,
                          int Hkv);
 

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     fa_paged_append,
     fa_paged_decode_noalloc,
     fa_paged_fwd,
+    fa_paged_num_splits,
     fa_selftest_wait_timeout,
     fa_paged_workspace_bytes,
     load_library,

@@ -25,7 +25,8 @@ _STATUS_NAMES = {
 
 EXPORTED = ("fa_status_string", "fa_fwd", "fa_paged_fwd", "fa_paged_workspace_bytes",
             "fa_decode_num_splits", "fa_merge_states", "fa_get_device_status", "fa_paged_decode_noalloc",
-            "fa_selftest_wait_timeout", "fa_paged_append", "fa_cascade_fwd", "fa_cascade_workspace_bytes")
+            "fa_selftest_wait_timeout", "fa_paged_append", "fa_cascade_fwd", "fa_cascade_workspace_bytes",
+            "fa_paged_num_splits")
 
 
 class FaError(RuntimeError):
@@ -61,6 +62,8 @@ def load_library(path: str = None) -> ctypes.CDLL:
     lib.fa_paged_fwd.restype = i
     lib.fa_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i, i]
     lib.fa_paged_workspace_bytes.restype = sz
+    lib.fa_paged_num_splits.argtypes = [i] * 9
+    lib.fa_paged_num_splits.restype = i
     lib.fa_decode_num_splits.argtypes = [i, i, i, i, i]
     lib.fa_decode_num_splits.restype = i
     lib.fa_merge_states.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
@@ -135,6 +138,12 @@ def fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages_
                              num_splits=0):
     return int(load_library().fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq,
                                                        num_pages, Hq, Hkv, d, num_splits))
+
+
+def fa_paged_num_splits(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d):
+    """Key splits fa_paged_fwd plans for these sizes with num_splits = 0 (1 = no split)."""
+    return load_library().fa_paged_num_splits(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages,
+                                              Hq, Hkv, d)
 
 
 def fa_decode_num_splits(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv):

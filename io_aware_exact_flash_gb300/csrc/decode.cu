@@ -340,12 +340,14 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
   }
 }
 
-// Merge of partial states, one CTA per row, 4 elements per thread:
+// Merge of partial states, one CTA per row, 4 elements per thread (bf16 output, or fp32 when
+// o_f32 is set):
 //   lse = log sum_p exp(lse_p),  O = sum_p exp(lse_p - lse) O_p.
 // A part with lse_p = -inf has no keys; its O_p is never read (it may hold any bits).
 template <bool LOG2>
 __global__ void merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int num_parts,
-                             int n_rows, int H, int D, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+                             int n_rows, int H, int D, __nv_bfloat16* __restrict__ o, float* __restrict__ o_f32,
+                             float* __restrict__ lse) {
   const int row = blockIdx.x;
   const int64_t out_row = row;
   const int per_head = D / 4;
@@ -369,10 +371,15 @@ __global__ void merge_kernel(const float* __restrict__ o_part, const float* __re
       }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2 packed;
-    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(o + (out_row * H + h) * D)[e4] = packed;
+    if (o_f32 != nullptr) {
+      reinterpret_cast<float4*>(o_f32 + (out_row * H + h) * D)[e4] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      reinterpret_cast<uint2*>(o + (out_row * H + h) * D)[e4] = packed;
+    }
     if (e4 == 0 && lse != nullptr) {
       float out = -INFINITY;
       if (wsum > 0.f) out = LOG2 ? (mx + __log2f(wsum)) * kLn2 : mx + __logf(wsum);
@@ -429,12 +436,12 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
 }
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H, int d, void* o,
-                         float* lse, bool log2_domain, cudaStream_t stream) {
+                         float* o_f32, float* lse, bool log2_domain, cudaStream_t stream) {
   auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
   if (log2_domain)
-    merge_kernel<true><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, lse);
+    merge_kernel<true><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
   else
-    merge_kernel<false><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, lse);
+    merge_kernel<false><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
   return cudaGetLastError();
 }
 

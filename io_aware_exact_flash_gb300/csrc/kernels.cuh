@@ -39,6 +39,12 @@ struct alignas(64) PrefillParams {
   const int32_t* cu_seqlens_q;
   const int32_t* kv_lens;
   int page_size, max_pages_per_seq, num_pages, num_seqs;
+  int pack;                // paged: query heads per tile row group (1, or the GQA group size:
+                           // a tile row is then (token, head of the group), 128 / pack tokens)
+  int kv_splits;           // paged: each unit's key tiles are split into this many contiguous
+                           // ranges, each a unit of its own writing an fp32 partial state
+  float* o_part;           // kv_splits > 1: fp32 [kv_splits, total_q, Hq, d] partial outputs
+  float* lse_part;         // kv_splits > 1: fp32 [kv_splits, total_q, Hq] partial LSEs (natural log)
   int64_t total_q;         // rows of q/o/lse; no row at or past it is ever written
   const int2* work_list;   // (sequence, query-tile pair) items, heaviest first
   const int* work_count;
@@ -102,6 +108,6 @@ cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, in
                                  int2* work_list, int* work_count, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H,
-                         int d, void* o, float* lse, bool log2_domain, cudaStream_t stream);
+                         int d, void* o, float* o_f32, float* lse, bool log2_domain, cudaStream_t stream);
 
 }  // namespace fa

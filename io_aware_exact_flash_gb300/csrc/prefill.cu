@@ -58,18 +58,22 @@ enum : uint32_t {
   kSiteMmaTurn = 8,
 };
 
-// One unit of work: a pair of 128-row query tiles of one (sequence, query head).
+// One unit of work: a pair of 128-row query tiles of one (sequence, query head), or, with GQA
+// packing (paged, pack > 1), of one (sequence, kv head): tile row r is then query token r / pack
+// of the tile and query head h + r % pack, so the pack heads sharing a kv head read each K/V tile
+// once, and a sequence with few query tokens (verify, decode rows) still fills the tile.
 struct Unit {
   int seq, h, hk, q_len, kv_len, off, nmax;
+  int split, kv_t0;   // paged key split: this unit's split and its first key tile
   int64_t tok0;  // token index of the sequence's first query row
   int nkv[kQTiles];   // key tiles per query tile; -1 = the tile has no query rows
-  int row0[kQTiles];  // first query row of each tile within its sequence
+  int row0[kQTiles];  // first (packed) row of each tile within its sequence
 };
 
 template <bool PAGED>
 __device__ __forceinline__ int count_units(const PrefillParams& p) {
   if constexpr (PAGED) {
-    return *p.work_count * p.Hq;
+    return *p.work_count * (p.Hq / p.pack) * p.kv_splits;
   } else {
     return ((p.S + 2 * kBM - 1) / (2 * kBM)) * p.B * p.Hq;
   }
@@ -80,8 +84,11 @@ template <bool PAGED>
 __device__ __forceinline__ void unit_at(const PrefillParams& p, int u, Unit& w) {
   int qt2;
   if constexpr (PAGED) {
-    const int item = u / p.Hq;
-    w.h = u % p.Hq;
+    const int slots = p.Hq / p.pack;
+    w.split = u % p.kv_splits;  // the splits of one tile pair are adjacent in the order
+    const int rest = u / p.kv_splits;
+    const int item = rest / slots;
+    w.h = (rest % slots) * p.pack;  // the first query head of the tile
     const int2 it = p.work_list[item];
     w.seq = it.x;
     qt2 = it.y;
@@ -110,21 +117,35 @@ __device__ __forceinline__ void unit_at(const PrefillParams& p, int u, Unit& w) 
     w.tok0 = (int64_t)w.seq * p.S;
     w.q_len = p.S;
     w.kv_len = p.S;
+    w.split = 0;
   }
   w.hk = w.h / p.group;
   w.off = w.kv_len - w.q_len;  // bottom-right causal alignment
   w.nmax = 0;
+  const int pack = PAGED ? p.pack : 1;
 #pragma unroll
   for (int g = 0; g < kQTiles; ++g) {
     w.row0[g] = qt2 * (2 * kBM) + g * kBM;
-    if (w.row0[g] >= w.q_len) {
+    if (w.row0[g] >= w.q_len * pack) {
       w.nkv[g] = -1;
     } else {
-      const int last = min(w.row0[g] + kBM - 1, w.q_len - 1);
+      const int last = min(w.row0[g] + kBM - 1, w.q_len * pack - 1) / pack;  // last query token
       const int lim = p.causal ? min(w.kv_len, last + w.off + 1) : w.kv_len;
       w.nkv[g] = lim > 0 ? (lim + kBN - 1) / kBN : 0;
     }
     w.nmax = max(w.nmax, w.nkv[g]);
+  }
+  w.kv_t0 = 0;
+  if (PAGED && p.kv_splits > 1) {
+    // split s takes key tiles [s * per, (s + 1) * per) of what each query tile needs
+    const int per = ((w.kv_len + kBN - 1) / kBN + p.kv_splits - 1) / p.kv_splits;
+    w.kv_t0 = w.split * per;
+    w.nmax = 0;
+#pragma unroll
+    for (int g = 0; g < kQTiles; ++g) {
+      if (w.nkv[g] >= 0) w.nkv[g] = max(0, min(w.nkv[g] - w.kv_t0, per));
+      w.nmax = max(w.nmax, w.nkv[g]);
+    }
   }
 }
 
@@ -300,7 +321,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 #pragma unroll
         for (int g = 0; g < kQTiles; ++g) {
           if (w.nkv[g] <= 0) continue;
-          const int qrow = PAGED ? (int)(w.tok0 + w.row0[g]) : w.row0[g];
+          const int qrow = PAGED ? (int)(w.tok0 + w.row0[g] / p.pack) : w.row0[g];
           const int qbat = PAGED ? 0 : w.seq;
 #pragma unroll
           for (int sub = 0; sub < C::kSub; ++sub)
@@ -319,7 +340,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                                            : p.num_pages;  // past the pool: TMA fills zeros
       };
       int phys_cur = 0, phys_next = 0;
-      if (PAGED && lane < ppt && w.nmax > 0) phys_cur = page_id(0);
+      if (PAGED && lane < ppt && w.nmax > 0) phys_cur = page_id(w.kv_t0);
       for (int idx = 0; idx < 2 * w.nmax; ++idx, ++kv_it) {
         const int j = idx >> 1;
         const bool is_v = idx & 1;
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
               tma_load_4d_hint(dst + sub * C::kSubBytes + lane * p.page_size * 128, tm, &bar_full[stage],
                                sub * 64, w.hk, 0, phys_cur, kv_policy);
             if (!is_v) {
-              phys_next = page_id(j + 1);
+              phys_next = page_id(w.kv_t0 + j + 1);
             } else {
               phys_cur = phys_next;
             }
@@ -430,7 +451,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
               // Rows of the sequence's partial last page past kv_len hold no valid value (possibly
               // not even a finite one); P is 0 there but 0 * NaN is NaN, so they are zeroed first.
               // Both issuers write the same zeros, each before its own P V.
-              const int t0 = j * kBN;
+              const int t0 = (w.kv_t0 + j) * kBN;
               if (t0 < w.kv_len && w.kv_len < t0 + kBN && (w.kv_len % p.page_size) != 0) {
                 const int r_begin = w.kv_len - t0;
                 const int r_end = min(kBN, ((w.kv_len + p.page_size - 1) / p.page_size) * p.page_size - t0);
@@ -512,7 +533,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       unit_at<PAGED>(p, u, w);
       const int nkv = g == 0 ? w.nkv[0] : w.nkv[1];
       if (nkv < 0) continue;
-      const int row = (g == 0 ? w.row0[0] : w.row0[1]) + r_in;
+      const int prow = (g == 0 ? w.row0[0] : w.row0[1]) + r_in;  // packed row of this thread
+      const int pack = PAGED ? p.pack : 1;
+      const int row = prow / pack;                                   // query token in the sequence
+      const int head = w.h + prow % pack;
       const int lim_row = p.causal ? min(w.kv_len, row + w.off + 1) : w.kv_len;  // keys [0, lim_row)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nkv; ++j, ++tcnt) {
@@ -528,7 +552,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         tmem_ld_wait(sr + 32);
         tmem_ld_wait(sr + 64);
         tmem_ld_wait(sr + 96);
-        const int valid = lim_row - j * kBN;
+        const int valid = lim_row - (w.kv_t0 + j) * kBN;
         if (valid < kBN) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
@@ -579,14 +603,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const int64_t tok = w.tok0 + row;
       const bool store = row < w.q_len && (!PAGED || tok < p.total_q);
-      if (store && p.o_f32 != nullptr) {
-        float4* dst = reinterpret_cast<float4*>(p.o_f32 + (tok * p.Hq + w.h) * D);
+      // a split unit writes its fp32 partial state into its split's part
+      float* o_f32 = p.o_f32;
+      float* lse_out = p.lse;
+      int64_t orow = tok * p.Hq + head;
+      if (PAGED && p.kv_splits > 1) {
+        o_f32 = p.o_part;
+        lse_out = p.lse_part;
+        orow += (int64_t)w.split * p.total_q * p.Hq;
+      }
+      if (store && o_f32 != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(o_f32 + orow * D);
 #pragma unroll
         for (int i = 0; i < D / 4; ++i)
           dst[i] = make_float4(u2f(orr[4 * i + 0]) * inv_l, u2f(orr[4 * i + 1]) * inv_l,
                                u2f(orr[4 * i + 2]) * inv_l, u2f(orr[4 * i + 3]) * inv_l);
       } else if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + w.h) * D);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow * D);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i)
           dst[i] = make_uint4(pack_bf16x2(u2f(orr[8 * i + 0]) * inv_l, u2f(orr[8 * i + 1]) * inv_l),
@@ -594,8 +627,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                               pack_bf16x2(u2f(orr[8 * i + 4]) * inv_l, u2f(orr[8 * i + 5]) * inv_l),
                               pack_bf16x2(u2f(orr[8 * i + 6]) * inv_l, u2f(orr[8 * i + 7]) * inv_l));
       }
-      if (store && p.lse != nullptr)
-        p.lse[tok * p.Hq + w.h] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      if (store && lse_out != nullptr) lse_out[orow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
       __syncwarp();
     }
   }
@@ -613,7 +645,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 // contiguous, heaviest query tiles first, so the CTAs running together share one sequence's
 // K/V pages in L2 while the order still starts with the longest work.
 __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ kv_lens,
-                                  int num_seqs, int causal, int max_cost, int max_items,
+                                  int num_seqs, int causal, int pack, int max_cost, int max_items,
                                   int2* __restrict__ work_list, int* __restrict__ work_count,
                                   int* __restrict__ order) {
   extern __shared__ int hist[];  // max_cost + 1 buckets
@@ -641,7 +673,7 @@ __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t*
       const int s = order[k];
       const int q_len = cu[s + 1] - cu[s];
       order[num_seqs + k] = items;  // first item of the k-th sequence in the order
-      items += q_len > 0 ? (q_len + 2 * kBM - 1) / (2 * kBM) : 0;
+      items += q_len > 0 ? (q_len * pack + 2 * kBM - 1) / (2 * kBM) : 0;
     }
     total = min(items, max_items);  // more items than the host bound means inconsistent lengths
     *work_count = total;
@@ -650,7 +682,7 @@ __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t*
   for (int k = tid; k < num_seqs; k += nt) {
     const int s = order[k];
     const int q_len = cu[s + 1] - cu[s];
-    const int n = q_len > 0 ? (q_len + 2 * kBM - 1) / (2 * kBM) : 0;
+    const int n = q_len > 0 ? (q_len * pack + 2 * kBM - 1) / (2 * kBM) : 0;
     const int base = order[num_seqs + k];
     for (int it = 0; it < n; ++it) {
       const int pos = base + it;
@@ -726,11 +758,11 @@ cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, in
                                  int2* work_list, int* work_count, cudaStream_t stream) {
   const int smem = (max_kv_tiles + 1) * (int)sizeof(int);
   int* order = reinterpret_cast<int*>(work_list + max_items);  // 2 * num_seqs ints of scratch
-  plan_paged_kernel<<<1, 1024, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, max_kv_tiles,
-                                              max_items, work_list, work_count, order);
+  plan_paged_kernel<<<1, 1024, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, p.pack,
+                                              max_kv_tiles, max_items, work_list, work_count, order);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long units = (long long)max_items * p.Hq;
+  const long long units = (long long)max_items * (p.Hq / p.pack) * p.kv_splits;
   const bool persistent = persistent_override() != 0;
   const int grid = (int)((units < sm_count || !persistent) ? units : sm_count);
   if (d == 128) return launch_prefill_impl<128, true>(p, grid, stream);

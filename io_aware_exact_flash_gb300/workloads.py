@@ -138,6 +138,13 @@ class PagedWorkload:
     decode: bool          # True: one query token per sequence; False: q_len = kv_len
     seed: int
     lengths: list = field(default=None)  # explicit kv lengths override the random draw
+    # query lengths other than "all of kv_len" (prefill) or 1 (decode); each sequence's queries
+    # are its last q_len tokens:
+    q_lo: int = 0         # q_hi > 0: q_len ~ U[q_lo, q_hi], at most kv_len (multi-token verify)
+    q_hi: int = 0
+    mix: tuple = None     # (n_full, n_chunk, chunk_lo, chunk_hi): n_full sequences with
+    #                       q_len = kv_len, n_chunk with q_len ~ U[chunk_lo, chunk_hi] (at most
+    #                       kv_len), the rest q_len = 1; roles from a seeded permutation
 
     @property
     def scale(self) -> float:
@@ -152,6 +159,15 @@ def paged_layout(w: PagedWorkload):
     else:
         kv_lens = g.integers(w.len_lo, w.len_hi + 1, size=w.num_seqs).astype(np.int32)
     q_lens = np.ones_like(kv_lens) if w.decode else kv_lens.copy()
+    if w.mix is not None:
+        n_full, n_chunk, lo, hi = w.mix
+        roles = g.permutation(len(kv_lens))
+        q_lens = np.ones_like(kv_lens)
+        q_lens[roles[:n_full]] = kv_lens[roles[:n_full]]
+        chunk = roles[n_full:n_full + n_chunk]
+        q_lens[chunk] = np.minimum(g.integers(lo, hi + 1, size=len(chunk)), kv_lens[chunk])
+    elif w.q_hi > 0:
+        q_lens = np.minimum(g.integers(w.q_lo, w.q_hi + 1, size=len(kv_lens)), kv_lens).astype(np.int32)
     cu = np.zeros(len(kv_lens) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(q_lens)
     pages_per_seq = (kv_lens + w.page_size - 1) // w.page_size
@@ -278,6 +294,15 @@ WORKLOADS = {
     "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16": PagedWorkload(
         "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16", num_seqs=128, len_lo=1024,
         len_hi=16384, Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=True, seed=1004),
+    # one launch mixing full prefill (16 seqs), chunked prefill (16 seqs, chunks of 1..512 new
+    # tokens behind their cached keys) and decode (32 seqs), kv_len 512..8192
+    "mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16": PagedWorkload(
+        "mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16", num_seqs=64, len_lo=512, len_hi=8192,
+        Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=False, seed=1006, mix=(16, 16, 1, 512)),
+    # speculative-decoding verification: 2..8 draft tokens per sequence behind 1024..16384 keys
+    "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16": PagedWorkload(
+        "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16", num_seqs=128, len_lo=1024,
+        len_hi=16384, Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=False, seed=1007, q_lo=2, q_hi=8),
     # 128 decode sequences behind one shared 16384-token prefix, own suffixes of 256..2048 tokens
     "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16": CascadeWorkload(
         "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16", num_seqs=128, prefix_len=16384,

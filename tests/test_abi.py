@@ -99,9 +99,17 @@ def test_workspace_query_is_host_only(lib):
 
     n_prefill = binding.fa_paged_workspace_bytes(64, 300000, 8192, 16, 512, 20000, 32, 8, 128)
     assert n_prefill >= 8 * (300000 // 256 + 64)
-    assert binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 32, 8, 128, num_splits=1) == 0
+    # decode with a GQA group of 4 runs on the tensor-core path: a work list, plus fp32 partial
+    # states when the keys are split
+    n1 = binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 32, 8, 128, num_splits=1)
+    assert 0 < n1 < 64 * 32 * 128 * 4
     n4 = binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 32, 8, 128, num_splits=4)
-    assert n4 >= 4 * 64 * 32 * (128 + 1) * 4
+    assert n4 >= n1 + 4 * 64 * 32 * (128 + 1) * 4
+    # decode without a GQA group of 2/4/8 runs on the split-KV CUDA-core kernel: one split needs
+    # no workspace, more need the partials
+    assert binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=1) == 0
+    n4 = binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=4)
+    assert n4 >= 4 * 64 * 8 * (128 + 1) * 4
 
 
 def test_merge_host_validation(lib):

@@ -162,3 +162,64 @@ def test_paged_decode_full_size():
     o, lse = run_paged(t, True, w.scale, num_splits=0)
     o_ref, lse_ref = oracle_paged(t, True, w.scale)
     compare(o, o_ref, lse, lse_ref, "decode full size")
+
+
+def test_mixed_batch_prefill_chunks_and_decode():
+    """One launch over a batch mixing full prefill (q_len = kv_len), chunked prefill (a few new
+    tokens behind cached keys) and decode rows (q_len = 1), bottom-right causal."""
+    lengths = [300, 1, 77, 1000, 129, 16, 2048, 5, 513, 64]
+    q_lens = [300, 1, 1, 129, 1, 16, 1, 3, 257, 1]
+    t = build_case(lengths, 8, 2, 128, 16, False, 61, q_lens=q_lens, extra_pages=2)
+    for causal in (True, False):
+        o, lse = run_paged(t, causal, 0.09)
+        o_ref, lse_ref = oracle_paged(t, causal, 0.09)
+        compare(o, o_ref, lse, lse_ref, f"mixed batch causal={causal}")
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 8, 2)])
+def test_multi_token_verify(d, Hq, Hkv):
+    """Speculative-decoding verification: 2..8 query tokens at the end of every sequence, each
+    seeing the cached keys and the draft tokens before it."""
+    lengths = [2, 8, 9, 100, 1024, 3000, 777, 16]
+    q_lens = [2, 8, 3, 5, 8, 7, 2, 6]
+    t = build_case(lengths, Hq, Hkv, d, 16, False, 71 + d, q_lens=q_lens)
+    o, lse = run_paged(t, True, 1 / math.sqrt(d))
+    o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(d))
+    compare(o, o_ref, lse, lse_ref, f"verify d={d} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("name", ["mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16",
+                                  "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16"])
+def test_mixed_and_verify_workloads_full_size(name):
+    """The mixed and verify workloads at full size in the benchmark's launch configuration:
+    every query token of the verify batch (four random heads each), and sampled rows (first,
+    last, random of each sequence) of the mixed batch, against the oracle."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    w = WORKLOADS[name]
+    t = make_paged(w)
+    o, lse = fa.fa_paged_fwd(to_dev(t["q"]), to_dev(t["k_pages"]), to_dev(t["v_pages"]), i32_dev(t["page_table"]),
+                             i32_dev(t["cu_seqlens_q"]), i32_dev(t["kv_lens"]), max_q_len=int(t["q_lens"].max()),
+                             causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == (0, 0)
+    cu = t["cu_seqlens_q"]
+    rng = np.random.default_rng(2)
+    if w.q_hi > 0:
+        # every query token, four of its heads
+        tok = np.repeat(np.arange(t["total_q"]), 4)
+        rows = np.stack([tok, rng.integers(0, w.Hq, len(tok))], axis=1).astype(np.int64)
+    else:
+        rows = []
+        for s in range(w.num_seqs):
+            for i in (0, int(t["q_lens"][s]) - 1, int(rng.integers(t["q_lens"][s]))):
+                rows.append((int(cu[s]) + i, int(rng.integers(w.Hq))))
+        rows = np.array(rows, np.int64)
+    o_ref, lse_ref = oracle.get().paged_rows(t["q"], t["k_pages"], t["v_pages"], t["page_table"], cu, t["kv_lens"],
+                                             True, w.scale, rows)
+    ridx = torch.from_numpy(rows).cuda()
+    compare(bf16_to_f64(o[ridx[:, 0], ridx[:, 1]]), o_ref, lse[ridx[:, 0], ridx[:, 1]].cpu().numpy(), lse_ref,
+            f"{name} full size")
+    assert bool(torch.isfinite(o.float()).all())
