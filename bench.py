@@ -54,8 +54,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one headline prefill launch from the ncu capture summarised in
 # profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on; the
 # bench reports it as roofline.traffic only while the kernel source is unchanged since then.
-PREFILL_TRAFFIC = {"bytes": 440380928 + 111717376,
-                   "source_sha256": "4792caa7df090cebbfc4ce1d7869c99f081b63eda7af426adbd7c41353e2e419"}
+PREFILL_TRAFFIC = {"bytes": 442331648 + 111583744,
+                   "source_sha256": "df15098e023303ccdda5160c85b8627fc7608fa6fa126d6a5231ce6ced871215"}
 L2_FLUSH_BYTES = 512 << 20
 
 
