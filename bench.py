@@ -380,36 +380,64 @@ def time_case(case, steps, warmup, flush):
 
 def e2e_dense(case, steps, warmup, device):
     """Headline metric through the public API with host buffers: every step copies q, k, v from
-    pinned host memory, runs the forward and copies O and LSE back."""
+    pinned host memory, runs the forward and copies O and LSE back to pinned host memory. The
+    copies run on their own streams with two device buffer sets, so step i+1's upload overlaps
+    step i's forward and download (the two copy directions use separate links); every step still
+    moves all of its inputs and results. Returns (ms per step, h2d bytes, d2h bytes per step)."""
     import torch
 
     import io_aware_exact_flash_gb300 as fa
 
     hq, hk, hv = (case.q.cpu().pin_memory(), case.k.cpu().pin_memory(), case.v.cpu().pin_memory())
-    ho = torch.empty(case.o.shape, dtype=case.o.dtype).pin_memory()
-    hl = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
+    ho = [torch.empty(case.o.shape, dtype=case.o.dtype).pin_memory() for _ in range(2)]
+    hl = [torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory() for _ in range(2)]
+    dev_in = [tuple(torch.empty_like(t) for t in (case.q, case.k, case.v)) for _ in range(2)]
+    dev_out = [(torch.empty_like(case.o), torch.empty_like(case.lse)) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    s_comp = torch.cuda.current_stream(device)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):  # every buffer starts free
+        in_free[b].record(s_comp)
+        out_free[b].record(s_out)
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        o, lse = fa.fa_fwd(dq, dk, dv, causal=case.w.causal, scale=case.w.scale, out=case.o, lse=case.lse)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+    def step(i):
+        b = i & 1
+        dq, dk, dv = dev_in[b]
+        do, dl = dev_out[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(in_free[b])      # the forward that last read this buffer is done
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            in_ready[b].record(s_in)
+        s_comp.wait_event(in_ready[b])
+        s_comp.wait_event(out_free[b])       # the download that last read these outputs is done
+        fa.fa_fwd(dq, dk, dv, causal=case.w.causal, scale=case.w.scale, out=do, lse=dl, stream=s_comp)
+        in_free[b].record(s_comp)
+        out_ready[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(out_ready[b])
+            ho[b].copy_(do, non_blocking=True)
+            hl[b].copy_(dl, non_blocking=True)
+            out_free[b].record(s_out)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        step()
-    end.record()
-    torch.cuda.synchronize()
+    start.record(s_comp)
+    s_in.wait_event(start)
+    for i in range(steps):
+        step(i)
+    s_comp.wait_stream(s_out)
+    end.record(s_comp)
+    torch.cuda.synchronize(device)
     ms = start.elapsed_time(end) / steps
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
     return ms, h2d, d2h
 
 
