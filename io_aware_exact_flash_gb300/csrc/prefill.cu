@@ -538,10 +538,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       const int row = prow / pack;                                   // query token in the sequence
       const int head = w.h + prow % pack;
       const int lim_row = p.causal ? min(w.kv_len, row + w.off + 1) : w.kv_len;  // keys [0, lim_row)
+      // A warp none of whose rows is a query row of the unit (the padding of a packed tile with
+      // few tokens) keeps every barrier phase but does no work: MMA rows are independent, and
+      // its rows' P and O are never stored.
+      const bool live = __any_sync(0xffffffffu, row < w.q_len);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nkv; ++j, ++tcnt) {
         mbar_wait(&bar_s[g], tcnt & 1, abort, p.status, kSiteSoftmaxS);
         __syncwarp();  // lanes leave the wait at different times; tcgen05.ld is warp-collective
+        if (!live) {
+          mbar_arrive(&bar_p[g]);
+          continue;
+        }
         tc_fence_after();
         uint32_t sr[kBN];
         tmem_ld32(tS + 0, sr + 0);
@@ -588,6 +596,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       if (nkv > 0) {
         mbar_wait(&bar_o[g], ounits & 1, abort, p.status, kSiteSoftmaxO);
         __syncwarp();
+        ++ounits;
+        if (!live) {
+          mbar_arrive(&bar_o_free[g]);
+          continue;
+        }
         tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, orr + cc * 32);
@@ -595,7 +608,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(orr + cc * 32);
         tc_fence_before();
         mbar_arrive(&bar_o_free[g]);  // the MMA may now overwrite O with the next unit
-        ++ounits;
       } else {
 #pragma unroll
         for (int i = 0; i < D; ++i) orr[i] = 0u;
