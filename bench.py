@@ -241,7 +241,8 @@ class PagedCase:
                                              t["page_table"].shape[1], t["num_pages"], self.w.Hq, self.w.Hkv,
                                              self.w.d)
         g = self.w.Hq // self.w.Hkv
-        self.tensor_cores = not (self.w.decode and g not in (2, 4, 8))
+        # decode runs on the tensor cores unless FA_DECODE_TC=0 sends it to the CUDA-core kernel
+        self.tensor_cores = not (self.w.decode and os.environ.get("FA_DECODE_TC") == "0" and g in (1, 2, 4, 8))
 
     def run(self):
         import io_aware_exact_flash_gb300 as fa

@@ -77,10 +77,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  *   kv_lens:       [num_seqs] int32 key/value lengths, 0 <= kv_len <= max_pages_per_seq*page_size;
  *   lse:           [total_q, Hq] fp32 or NULL.
  *   max_q_len:     the largest query length (a host-side bound, used for planning).
- *                  Batches run on the tiled tensor-core kernel; with a GQA group (Hq / Hkv) of
- *                  2, 4 or 8 the group's query heads share each tile (rows = token x head), so
- *                  decode and multi-token verify rows fill the tensor core too. A decode batch
- *                  (max_q_len == 1) with any other group runs on a split-KV CUDA-core kernel.
+ *                  Batches run on the tiled tensor-core kernel; when the GQA group (Hq / Hkv) is
+ *                  a power of two from 2 to 128 (MQA included) the group's query heads share
+ *                  each tile (rows = token x head), so decode and multi-token verify rows fill
+ *                  the tensor core too (decode included: it stays bound by reading K/V).
  *   num_splits:    key splits: each sequence's keys are cut into num_splits contiguous ranges,
  *                  attended in parallel as fp32 partial states and merged by their LSE. 0 chooses
  *                  from the SM count (splits only when there is too little other parallelism).
@@ -107,7 +107,8 @@ int fa_paged_num_splits(int num_seqs, int total_q, int max_q_len, int page_size,
                         int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d);
 
 /* The split count the split-KV CUDA-core decode kernel uses for a decode batch with these sizes
- * (num_splits = 0): the path of decode batches whose GQA group is not 2, 4 or 8. */
+ * (num_splits = 0). That kernel serves fa_paged_decode_noalloc, and fa_paged_fwd's decode batches
+ * when the environment variable FA_DECODE_TC is 0. */
 int fa_decode_num_splits(int num_seqs, int page_size, int max_pages_per_seq, int num_pages,
                          int Hkv);
 
@@ -190,7 +191,9 @@ fa_status fa_paged_append(const void* k_new, const void* v_new, const int32_t* c
  * example an engine whose device memory is all handed to a fixed arena, or a plugin inside a
  * host that owns every allocation) and so cannot lend fa_paged_fwd a workspace.
  *   Arguments and results are those of fa_paged_fwd for a decode batch (every query length is
- *   0 or 1, i.e. max_q_len == 1); inputs and outputs are still the caller's.
+ *   0 or 1, i.e. max_q_len == 1); inputs and outputs are still the caller's. It always runs the
+ *   split-KV CUDA-core decode kernel, which takes GQA groups (Hq / Hkv) of 1, 2, 4 and 8; other
+ *   groups return FA_ERR_UNSUPPORTED.
  *   Scratch: the per-split partials live in a fixed device array of FA_NOALLOC_SCRATCH_BYTES
  *   (16 MiB) inside this library, which every GPU that loads the library holds until the process
  *   exits. The function itself allocates and frees nothing.

@@ -137,9 +137,7 @@ DecodePlan plan_decode(int num_seqs, int page_size, int max_pages_per_seq, int n
   return d;
 }
 
-// Work items (tile pairs) of a paged prefill launch are at most total_q * pack / 256 + num_seqs;
-// the workspace is sized for the largest packing (8 rows per token).
-constexpr int kMaxPack = 8;
+// Work items (tile pairs) of a paged prefill launch are at most total_q * pack / 256 + num_seqs.
 int prefill_max_items(int num_seqs, int total_q, int pack) {
   return (int)((long long)total_q * pack / 256) + num_seqs;
 }
@@ -149,8 +147,8 @@ size_t decode_workspace(int num_seqs, int Hq, int Hkv, int d, int splits) {
 }
 
 // count | work list (int2 per item) | sequence order and item offsets (2 ints per sequence)
-size_t prefill_workspace(int num_seqs, int total_q) {
-  return 256 + align_up((size_t)prefill_max_items(num_seqs, total_q, kMaxPack) * sizeof(int2) +
+size_t prefill_workspace(int num_seqs, int total_q, int pack) {
+  return 256 + align_up((size_t)prefill_max_items(num_seqs, total_q, pack) * sizeof(int2) +
                             2 * sizeof(int) * num_seqs,
                         256);
 }
@@ -219,27 +217,31 @@ int env_switch(const char* name, int* cache) {
   return *cache;
 }
 
+bool pow2_group(int group) { return group >= 2 && group <= fa::kBM && (group & (group - 1)) == 0; }
+
 // GQA packing of the paged tensor-core path: the query heads that share a kv head fill one tile
-// together (rows = token x head), so every K/V tile is read once for the whole group and
-// sequences with few query tokens (multi-token verify, decode rows of a mixed batch) fill their
-// tiles instead of holding a handful of rows. Measured faster on every paged workload with
-// group 4 (long ragged prefill +3%, mixed batch +15%, verify 3.7x), so it is the default for
-// groups of 2, 4 and 8. FA_PAGED_PACK=0 turns it off.
+// together (rows = token x head, 128 / group tokens), so every K/V tile is read once for the
+// whole group and sequences with few query tokens (multi-token verify, decode rows of a mixed
+// batch) fill their tiles instead of holding a handful of rows. Measured faster on every paged
+// workload with group 4 (long ragged prefill +3%, mixed batch +15%, verify 3.7x), so it is the
+// default for every power-of-two group up to 128 (MQA included). FA_PAGED_PACK=0 turns it off.
 int choose_pack(int group, int max_q_len) {
   (void)max_q_len;
-  if (group != 2 && group != 4 && group != 8) return 1;
+  if (!pow2_group(group)) return 1;
   static int mode = -2;
   return env_switch("FA_PAGED_PACK", &mode) == 0 ? 1 : group;
 }
 
-// Decode batches (one query row per sequence) with a GQA group of 2, 4 or 8 run on the packed
-// tensor-core path: a tile holds every query head of a kv head, and the MMAs cost far less than
-// streaming the keys, so the path is bound by reading K/V (measured 5410 vs 4683 GB/s on 128
-// sequences, 3999 vs 3097 on 32). Other groups use the split-KV CUDA-core kernel; FA_DECODE_TC=0
-// sends every decode batch there.
+// Decode batches (one query row per sequence) run on the tensor-core path: with a packed group a
+// tile holds every query head of a kv head, and in any case the MMAs cost far less than streaming
+// the keys, so the path is bound by reading K/V. Measured against the split-KV CUDA-core kernel:
+// group 4, 128 sequences 5410 vs 4683 GB/s, 32 sequences 3999 vs 3097; MHA (group 1, one real
+// row per tile), 32 sequences 5501 vs 4501. FA_DECODE_TC=0 sends groups 1, 2, 4 and 8 (the
+// groups that kernel takes) to the CUDA-core kernel.
 bool decode_on_tensor_cores(int group) {
   static int mode = -2;
-  return (group == 2 || group == 4 || group == 8) && env_switch("FA_DECODE_TC", &mode) != 0;
+  if (group == 1 || group == 2 || group == 4 || group == 8) return env_switch("FA_DECODE_TC", &mode) != 0;
+  return true;
 }
 
 // Key splits of the paged tensor-core path. Each (tile pair, head slot) unit becomes kv_splits
@@ -293,7 +295,7 @@ size_t paged_pass_workspace(int num_seqs, int total_q, int max_q_len, int page_s
   const int pack = choose_pack(group, max_q_len);
   const int splits = plan_kv_splits(num_seqs, total_q, max_q_len, pack, Hq, d,
                                     max_kv_tiles_of(max_pages_per_seq, page_size), sm_count, num_splits);
-  return prefill_workspace(num_seqs, total_q) + split_parts_bytes(splits, total_q, Hq, d, nullptr);
+  return prefill_workspace(num_seqs, total_q, pack) + split_parts_bytes(splits, total_q, Hq, d, nullptr);
 }
 
 // Enqueue one validated paged pass. O goes to `o` as bf16, or to `o_f32` as fp32 when that is set.
@@ -346,7 +348,7 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   const int max_kv_tiles = max_kv_tiles_of(max_pages_per_seq, page_size);
   const int kv_splits =
       plan_kv_splits(num_seqs, total_q, max_q_len, pack, Hq, d, max_kv_tiles, dev->sm_count, num_splits);
-  const size_t list_bytes = prefill_workspace(num_seqs, total_q);
+  const size_t list_bytes = prefill_workspace(num_seqs, total_q, pack);
   size_t lse_off = 0;
   const size_t need = list_bytes + split_parts_bytes(kv_splits, total_q, Hq, d, &lse_off);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;

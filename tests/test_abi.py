@@ -105,11 +105,24 @@ def test_workspace_query_is_host_only(lib):
     assert 0 < n1 < 64 * 32 * 128 * 4
     n4 = binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 32, 8, 128, num_splits=4)
     assert n4 >= n1 + 4 * 64 * 32 * (128 + 1) * 4
-    # decode without a GQA group of 2/4/8 runs on the split-KV CUDA-core kernel: one split needs
-    # no workspace, more need the partials
-    assert binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=1) == 0
-    n4 = binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=4)
-    assert n4 >= 4 * 64 * 8 * (128 + 1) * 4
+    # MHA decode runs there too (one real row per tile)
+    assert binding.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=1) > 0
+
+
+def test_workspace_of_cuda_core_decode():
+    """With FA_DECODE_TC=0 decode batches of groups 1/2/4/8 run on the split-KV CUDA-core kernel:
+    one split needs no workspace, more need the partials (the switch is read once per process)."""
+    import subprocess
+    import sys
+
+    code = ("from io_aware_exact_flash_gb300 import binding as b\n"
+            "print(b.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=1),"
+            " b.fa_paged_workspace_bytes(64, 64, 1, 16, 512, 20000, 8, 8, 128, num_splits=4))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, FA_DECODE_TC="0"))
+    assert r.returncode == 0, r.stderr
+    n1, n4 = map(int, r.stdout.split())
+    assert n1 == 0 and n4 >= 4 * 64 * 8 * (128 + 1) * 4
 
 
 def test_merge_host_validation(lib):

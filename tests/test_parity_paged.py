@@ -80,7 +80,8 @@ def test_paged_prefill_page_sizes(page_size):
 
 
 @pytest.mark.parametrize("d,Hq,Hkv,causal", [(64, 4, 4, True), (128, 4, 1, False), (64, 8, 1, False),
-                                             (128, 6, 3, True)])
+                                             (128, 6, 3, True), (128, 32, 1, True), (64, 16, 1, False),
+                                             (128, 12, 4, True)])
 def test_paged_prefill_heads_and_dims(d, Hq, Hkv, causal):
     t = build_case([40, 700, 129, 1, 384], Hq, Hkv, d, 16, False, 5 + d + Hq)
     o, lse = run_paged(t, causal, 1 / math.sqrt(d))
@@ -99,7 +100,8 @@ def test_paged_prefill_query_shorter_than_keys():
 
 
 @pytest.mark.parametrize("splits", [1, 2, 7, 0])
-@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 8, 8), (128, 16, 2), (128, 8, 4)])
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 8, 8), (128, 16, 2), (128, 8, 4), (128, 32, 1),
+                                     (64, 12, 4), (128, 6, 1)])
 def test_paged_decode_splits(splits, d, Hq, Hkv):
     lengths = [1, 16, 17, 1000, 4096, 3333, 64, 250]
     t = build_case(lengths, Hq, Hkv, d, 16, True, 31 + d + Hq, extra_pages=2)
@@ -176,7 +178,7 @@ def test_mixed_batch_prefill_chunks_and_decode():
         compare(o, o_ref, lse, lse_ref, f"mixed batch causal={causal}")
 
 
-@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 8, 2)])
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 32, 1), (128, 12, 4)])
 def test_multi_token_verify(d, Hq, Hkv):
     """Speculative-decoding verification: 2..8 query tokens at the end of every sequence, each
     seeing the cached keys and the draft tokens before it."""
