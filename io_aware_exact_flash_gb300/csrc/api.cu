@@ -247,8 +247,10 @@ bool decode_on_tensor_cores(int group) {
 // Key splits of the paged tensor-core path. Each (tile pair, head slot) unit becomes kv_splits
 // units over contiguous key ranges, written as fp32 partial states and merged by their LSE
 // afterwards. Splitting pays when there are too few units to fill the GPU a few times over
-// (small decode batches, one long shared prefix); each split keeps at least 4 key tiles, and
-// the partial states are kept under 1 GiB. requested > 0 fixes the count (capped at the key
+// (small decode batches, one long shared prefix); each split keeps at least 8 key tiles, and
+// the partial states are kept under 1 GiB. (Targets of 2, 3, 4 and 6 waves with at least 4 or 8
+// tiles were measured on decode batches of 4 to 64 sequences and the cascade; 3 and 8 was best
+// or level everywhere.) requested > 0 fixes the count (capped at the key
 // tiles of the longest sequence).
 int plan_kv_splits(int num_seqs, int total_q, int max_q_len, int pack, int Hq, int d, int max_kv_tiles,
                    int sm_count, int requested) {
@@ -262,7 +264,7 @@ int plan_kv_splits(int num_seqs, int total_q, int max_q_len, int pack, int Hq, i
   const long long target = 3LL * sm_count;
   if (units <= 0 || units >= target) return 1;
   long long s = (target + units - 1) / units;
-  if (s > max_kv_tiles / 4) s = max_kv_tiles / 4;
+  if (s > max_kv_tiles / 8) s = max_kv_tiles / 8;
   const long long part = (long long)total_q * Hq * (d + 1) * 4;
   if (part > 0 && s * part > (1LL << 30)) s = (1LL << 30) / part;
   return s < 1 ? 1 : (int)s;
