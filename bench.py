@@ -54,8 +54,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one headline prefill launch from the ncu capture summarised in
 # profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on; the
 # bench reports it as roofline.traffic only while the kernel source is unchanged since then.
-PREFILL_TRAFFIC = {"bytes": 442331648 + 111583744,
-                   "source_sha256": "df15098e023303ccdda5160c85b8627fc7608fa6fa126d6a5231ce6ced871215"}
+PREFILL_TRAFFIC = {"bytes": 426887936 + 110245120,
+                   "source_sha256": "590dc2bf896988b279c909d6b8f05679028ba692aad4211a664273eafb3a3a93"}
 L2_FLUSH_BYTES = 512 << 20
 
 
