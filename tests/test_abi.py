@@ -66,6 +66,8 @@ def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=2, S=128,
     (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
     (dict(d=96), 2), (dict(d=256), 2),
     (dict(q=FAKE + 8), 3), (dict(v=FAKE + 2), 3), (dict(lse=FAKE + 2), 3),
+    (dict(B=1 << 12, S=1 << 20), 2),  # B * S rows past 2^31 - 1
+    (dict(B=1 << 10, S=1 << 20, Hq=1 << 10, Hkv=1 << 10), 2),  # elements past 2^40
 ])
 def test_fa_fwd_host_validation(lib, kw, code):
     assert _fwd(lib, **kw) == code
@@ -89,6 +91,8 @@ def _paged(lib, **kw):
     (dict(num_pages=0), 1), (dict(splits=-1), 1),
     (dict(ps=8), 2), (dict(ps=48), 2), (dict(d=80), 2),
     (dict(kp=FAKE + 4), 3), (dict(cu=FAKE + 2), 3),
+    (dict(max_pages=1 << 26, ps=32), 2),   # a sequence past 2^30 keys
+    (dict(num_pages=1 << 27, ps=32), 2),   # a pool past 2^31 - 1 rows
 ])
 def test_fa_paged_fwd_host_validation(lib, kw, code):
     assert _paged(lib, **kw) == code
