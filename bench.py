@@ -315,13 +315,13 @@ class CascadeCase:
         need_flat = fa.fa_paged_workspace_bytes(w.num_seqs, self.total_q, w.q_len, w.page_size,
                                                 t["flat_page_table"].shape[1], t["num_pages"], w.Hq, w.Hkv, w.d)
         self.ws_flat = torch.empty(max(need_flat, 256), dtype=torch.uint8, device=device)
-        # launches: each pass is planning + attention (+ a merge when its keys are split), then the
-        # merge of the two passes
+        # launches: each pass is planning + attention, the suffix pass also a merge when its keys
+        # are split; the prefix pass's key splits go straight into the final merge
         sp_pre = fa.fa_paged_num_splits(1, self.total_q, self.total_q, w.page_size, t["prefix_page_table"].shape[1],
                                         t["num_pages"], w.Hq, w.Hkv, w.d)
         sp_suf = fa.fa_paged_num_splits(w.num_seqs, self.total_q, w.q_len, w.page_size, t["page_table"].shape[1],
                                         t["num_pages"], w.Hq, w.Hkv, w.d)
-        self.launches = (2 + (sp_pre > 1)) + (2 + (sp_suf > 1)) + 1
+        self.launches = 2 + (2 + (sp_suf > 1)) + 1
         self.prefix_splits = sp_pre
         kv_rows = w.prefix_len + int(t["kv_lens"].astype(np.int64).sum())
         self.bytes = (2 * kv_rows * w.Hkv * w.d * 2 + self.total_q * w.Hq * w.d * 2 * 2 + self.total_q * w.Hq * 4)

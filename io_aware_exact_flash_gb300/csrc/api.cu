@@ -287,8 +287,20 @@ int max_kv_tiles_of(int max_pages_per_seq, int page_size) {
 }
 
 // Workspace of one paged pass (decode partials, or the prefill work list).
+// The key-split count of one paged pass (1 on the CUDA-core decode kernel, which merges its own).
+int paged_pass_splits(int num_seqs, int total_q, int max_q_len, int page_size, int max_pages_per_seq, int Hq, int Hkv,
+                      int d, int num_splits, int sm_count) {
+  const int group = Hkv > 0 ? Hq / Hkv : 0;
+  if (max_q_len == 1 && !decode_on_tensor_cores(group)) return 1;
+  return plan_kv_splits(num_seqs, total_q, max_q_len, choose_pack(group, max_q_len), Hq, d,
+                        max_kv_tiles_of(max_pages_per_seq, page_size), sm_count, num_splits);
+}
+
+// Workspace of one paged pass. external_parts: the pass writes its split partial states into the
+// caller's part arrays (no merge of its own), so they are not counted here.
 size_t paged_pass_workspace(int num_seqs, int total_q, int max_q_len, int page_size, int max_pages_per_seq,
-                            int num_pages, int Hq, int Hkv, int d, int num_splits, int sm_count) {
+                            int num_pages, int Hq, int Hkv, int d, int num_splits, int sm_count,
+                            bool external_parts = false) {
   const int group = Hkv > 0 ? Hq / Hkv : 0;
   if (max_q_len == 1 && !decode_on_tensor_cores(group)) {
     const DecodePlan dp = plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, sm_count);
@@ -297,7 +309,8 @@ size_t paged_pass_workspace(int num_seqs, int total_q, int max_q_len, int page_s
   const int pack = choose_pack(group, max_q_len);
   const int splits = plan_kv_splits(num_seqs, total_q, max_q_len, pack, Hq, d,
                                     max_kv_tiles_of(max_pages_per_seq, page_size), sm_count, num_splits);
-  return prefill_workspace(num_seqs, total_q, pack) + split_parts_bytes(splits, total_q, Hq, d, nullptr);
+  return prefill_workspace(num_seqs, total_q, pack) +
+         (external_parts ? 0 : split_parts_bytes(splits, total_q, Hq, d, nullptr));
 }
 
 // Enqueue one validated paged pass. O goes to `o` as bf16, or to `o_f32` as fp32 when that is set.
@@ -305,7 +318,8 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
                         const int32_t* page_table, const int32_t* cu_seqlens_q, const int32_t* kv_lens, int num_seqs,
                         int total_q, int max_q_len, int page_size, int max_pages_per_seq, int num_pages, int Hq,
                         int Hkv, int d, int causal, float scale, void* o, float* o_f32, float* lse, void* workspace,
-                        size_t workspace_bytes, int num_splits, fa_stream_t stream) {
+                        size_t workspace_bytes, int num_splits, fa_stream_t stream, float* ext_o_parts = nullptr,
+                        float* ext_lse_parts = nullptr) {
   if (total_q == 0) return FA_OK;
   const int group = Hq / Hkv;
 
@@ -351,8 +365,10 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   const int kv_splits =
       plan_kv_splits(num_seqs, total_q, max_q_len, pack, Hq, d, max_kv_tiles, dev->sm_count, num_splits);
   const size_t list_bytes = prefill_workspace(num_seqs, total_q, pack);
+  // ext_o_parts: split partial states go to the caller's part arrays, which it merges itself
+  const bool external = ext_o_parts != nullptr && kv_splits > 1;
   size_t lse_off = 0;
-  const size_t need = list_bytes + split_parts_bytes(kv_splits, total_q, Hq, d, &lse_off);
+  const size_t need = list_bytes + (external ? 0 : split_parts_bytes(kv_splits, total_q, Hq, d, &lse_off));
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
   fa::PrefillParams p;
@@ -394,7 +410,10 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   p.work_count = work_count;
   p.pack = pack;
   p.kv_splits = kv_splits;
-  if (kv_splits > 1) {
+  if (external) {
+    p.o_part = ext_o_parts;
+    p.lse_part = ext_lse_parts;
+  } else if (kv_splits > 1) {
     char* parts = static_cast<char*>(workspace) + list_bytes;
     p.o_part = reinterpret_cast<float*>(parts);
     p.lse_part = reinterpret_cast<float*>(parts + lse_off);
@@ -404,7 +423,7 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   if (fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q, pack), cost_buckets,
                                work_list, work_count, stream) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (kv_splits > 1 &&
+  if (kv_splits > 1 && !external &&
       fa::launch_merge(p.o_part, p.lse_part, kv_splits, total_q, Hq, d, o, o_f32, lse, false, stream) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
@@ -521,15 +540,15 @@ fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages, 
                        workspace_bytes, num_splits, stream);
 }
 
-// Shared-prefix (cascade) attention: the prefix pass and the suffix pass each leave an fp32 partial
-// state (O normalised over its own keys, natural-log LSE) in the workspace; the merge combines them.
-// Workspace: O parts [2, total_q, Hq, d] fp32 | LSE parts [2, total_q, Hq] fp32 | the passes' own
-// scratch (reused by both, which run one after the other on the stream).
+// Shared-prefix (cascade) attention: the prefix pass leaves one fp32 partial state per key split
+// (O normalised over its own keys, natural-log LSE), the suffix pass one more, and a single merge
+// combines them all. Workspace: O parts [parts, total_q, Hq, d] fp32 | LSE parts [parts, total_q,
+// Hq] fp32 | the passes' own scratch (reused by both, which run one after the other on the stream).
 namespace {
-size_t cascade_parts_bytes(int total_q, int Hq, int d, size_t* lse_offset) {
-  const size_t o_bytes = align_up((size_t)2 * total_q * Hq * d * sizeof(float), 256);
+size_t cascade_parts_bytes(int parts, int total_q, int Hq, int d, size_t* lse_offset) {
+  const size_t o_bytes = align_up((size_t)parts * total_q * Hq * d * sizeof(float), 256);
   if (lse_offset) *lse_offset = o_bytes;
-  return o_bytes + align_up((size_t)2 * total_q * Hq * sizeof(float), 256);
+  return o_bytes + align_up((size_t)parts * total_q * Hq * sizeof(float), 256);
 }
 }  // namespace
 
@@ -542,11 +561,12 @@ size_t fa_cascade_workspace_bytes(int num_groups, int num_seqs, int total_q, int
           FA_OK)
     return 0;
   const int sms = sm_count_now();
+  const int sp = paged_pass_splits(num_groups, total_q, max_group_q_len, page_size, max_prefix_pages, Hq, Hkv, d, 0, sms);
   const size_t a = paged_pass_workspace(num_groups, total_q, max_group_q_len, page_size, max_prefix_pages, num_pages,
-                                        Hq, Hkv, d, 0, sms);
+                                        Hq, Hkv, d, 0, sms, true);
   const size_t b =
       paged_pass_workspace(num_seqs, total_q, max_q_len, page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, 0, sms);
-  return cascade_parts_bytes(total_q, Hq, d, nullptr) + (a > b ? a : b);
+  return cascade_parts_bytes(sp + 1, total_q, Hq, d, nullptr) + (a > b ? a : b);
 }
 
 fa_status fa_cascade_fwd(const void* q, const void* k_pages, const void* v_pages, int page_size, int num_pages, int Hq,
@@ -575,26 +595,31 @@ fa_status fa_cascade_fwd(const void* q, const void* k_pages, const void* v_pages
                                                  max_prefix_pages, max_pages_per_seq, num_pages, Hq, Hkv, d);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+  const int sp = paged_pass_splits(num_groups, total_q, max_group_q_len, page_size, max_prefix_pages, Hq, Hkv, d, 0,
+                                   dev->sm_count);
   size_t lse_off = 0;
-  const size_t parts = cascade_parts_bytes(total_q, Hq, d, &lse_off);
+  const size_t parts = cascade_parts_bytes(sp + 1, total_q, Hq, d, &lse_off);
   char* base = static_cast<char*>(workspace);
   float* o_parts = reinterpret_cast<float*>(base);
   float* lse_parts = reinterpret_cast<float*>(base + lse_off);
   const size_t part_rows = (size_t)total_q * Hq;
   void* scratch = base + parts;
   const size_t scratch_bytes = workspace_bytes - parts;
-  // prefix pass: every query row of a group sees all of the group's shared keys
+  // prefix pass: every query row of a group sees all of the group's shared keys; its key splits
+  // (parts 0 .. sp-1) are left for the final merge
   err = enqueue_paged(dev, q, k_pages, v_pages, prefix_page_table, cu_q_groups, prefix_lens, num_groups, total_q,
                       max_group_q_len, page_size, max_prefix_pages, num_pages, Hq, Hkv, d, 0, scale, nullptr, o_parts,
-                      lse_parts, scratch, scratch_bytes, 0, stream);
+                      lse_parts, scratch, scratch_bytes, 0, stream, sp > 1 ? o_parts : nullptr,
+                      sp > 1 ? lse_parts : nullptr);
   if (err != FA_OK) return err;
-  // suffix pass: each sequence's own keys, with the caller's masking
+  // suffix pass: each sequence's own keys, with the caller's masking (part sp)
   err = enqueue_paged(dev, q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, num_seqs, total_q, max_q_len,
                       page_size, max_pages_per_seq, num_pages, Hq, Hkv, d, causal, scale, nullptr,
-                      o_parts + part_rows * d, lse_parts + part_rows, scratch, scratch_bytes, 0, stream);
+                      o_parts + part_rows * d * sp, lse_parts + part_rows * sp, scratch, scratch_bytes, 0, stream);
   if (err != FA_OK) return err;
-  return fa::launch_merge(o_parts, lse_parts, 2, total_q, Hq, d, o, nullptr, lse, false, stream) == cudaSuccess ? FA_OK
-                                                                                                      : FA_ERR_CUDA;
+  return fa::launch_merge(o_parts, lse_parts, sp + 1, total_q, Hq, d, o, nullptr, lse, false, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
 }
 
 fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_parts, int n_rows, int H, int d,

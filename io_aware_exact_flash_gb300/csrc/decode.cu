@@ -340,51 +340,54 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
   }
 }
 
-// Merge of partial states, one CTA per row, 4 elements per thread (bf16 output, or fp32 when
-// o_f32 is set):
+// Merge of partial states: grid (row, block of 128 (head, 4-column) items), one item per thread
+// (bf16 output, or fp32 when o_f32 is set):
 //   lse = log sum_p exp(lse_p),  O = sum_p exp(lse_p - lse) O_p.
-// A part with lse_p = -inf has no keys; its O_p is never read (it may hold any bits).
+// A part with lse_p = -inf has no keys; its O_p is never read (it may hold any bits). The loop over
+// parts is unrolled so several parts' loads are in flight at once.
 template <bool LOG2>
-__global__ void merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int num_parts,
-                             int n_rows, int H, int D, __nv_bfloat16* __restrict__ o, float* __restrict__ o_f32,
-                             float* __restrict__ lse) {
-  const int row = blockIdx.x;
-  const int64_t out_row = row;
+__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ o_part,
+                                                    const float* __restrict__ lse_part, int num_parts, int n_rows,
+                                                    int H, int D, __nv_bfloat16* __restrict__ o,
+                                                    float* __restrict__ o_f32, float* __restrict__ lse) {
+  const int64_t row = blockIdx.x;
   const int per_head = D / 4;
-  for (int t = threadIdx.x; t < H * per_head; t += blockDim.x) {
-    const int h = t / per_head, e4 = t % per_head;
-    float mx = -INFINITY;
-    for (int s = 0; s < num_parts; ++s) mx = fmaxf(mx, lse_part[((int64_t)s * n_rows + row) * H + h]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-      for (int s = 0; s < num_parts; ++s) {
-        const float ls = lse_part[((int64_t)s * n_rows + row) * H + h];
-        if (ls == -INFINITY) continue;
-        const float w = LOG2 ? ex2(ls - mx) : __expf(ls - mx);
-        const float4 v = reinterpret_cast<const float4*>(o_part + (((int64_t)s * n_rows + row) * H + h) * D)[e4];
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-        wsum += w;
-      }
+  const int t = blockIdx.y * blockDim.x + threadIdx.x;
+  if (t >= H * per_head) return;
+  const int h = t / per_head, e4 = t % per_head;
+  const int64_t lrow = row * H + h;                // (row, head) in one part
+  const int64_t pstride = (int64_t)n_rows * H;     // rows x heads of one part
+  float mx = -INFINITY;
+  for (int s = 0; s < num_parts; ++s) mx = fmaxf(mx, __ldg(&lse_part[s * pstride + lrow]));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll 4
+    for (int s = 0; s < num_parts; ++s) {
+      const float ls = __ldg(&lse_part[s * pstride + lrow]);
+      if (ls == -INFINITY) continue;
+      const float w = LOG2 ? ex2(ls - mx) : __expf(ls - mx);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(o_part + (s * pstride + lrow) * D) + e4);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+      wsum += w;
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    if (o_f32 != nullptr) {
-      reinterpret_cast<float4*>(o_f32 + (out_row * H + h) * D)[e4] =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    } else {
-      uint2 packed;
-      packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      reinterpret_cast<uint2*>(o + (out_row * H + h) * D)[e4] = packed;
-    }
-    if (e4 == 0 && lse != nullptr) {
-      float out = -INFINITY;
-      if (wsum > 0.f) out = LOG2 ? (mx + __log2f(wsum)) * kLn2 : mx + __logf(wsum);
-      lse[out_row * H + h] = out;
-    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  if (o_f32 != nullptr) {
+    reinterpret_cast<float4*>(o_f32 + lrow * D)[e4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  } else {
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(o + lrow * D)[e4] = packed;
+  }
+  if (e4 == 0 && lse != nullptr) {
+    float out = -INFINITY;
+    if (wsum > 0.f) out = LOG2 ? (mx + __log2f(wsum)) * kLn2 : mx + __logf(wsum);
+    lse[lrow] = out;
   }
 }
 
@@ -438,10 +441,11 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H, int d, void* o,
                          float* o_f32, float* lse, bool log2_domain, cudaStream_t stream) {
   auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
+  const dim3 grid((unsigned)n_rows, (unsigned)((H * (d / 4) + 127) / 128));
   if (log2_domain)
-    merge_kernel<true><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
+    merge_kernel<true><<<grid, 128, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
   else
-    merge_kernel<false><<<n_rows, 256, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
+    merge_kernel<false><<<grid, 128, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
   return cudaGetLastError();
 }
 
