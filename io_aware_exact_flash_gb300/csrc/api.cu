@@ -364,6 +364,9 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   const int max_kv_tiles = max_kv_tiles_of(max_pages_per_seq, page_size);
   const int kv_splits =
       plan_kv_splits(num_seqs, total_q, max_q_len, pack, Hq, d, max_kv_tiles, dev->sm_count, num_splits);
+  // units (tile pairs x head slots x key splits) are counted in 32-bit integers on the device
+  if ((long long)prefill_max_items(num_seqs, total_q, pack) * (Hq / pack) * kv_splits >= (1LL << 31))
+    return FA_ERR_UNSUPPORTED;
   const size_t list_bytes = prefill_workspace(num_seqs, total_q, pack);
   // ext_o_parts: split partial states go to the caller's part arrays, which it merges itself
   const bool external = ext_o_parts != nullptr && kv_splits > 1;
