@@ -4,16 +4,20 @@
 // its page table ("I/O-Aware Kernels", datasystem.school Module 5, section "FlashInfer: I/O-aware
 // attention for serving"). Every key/value byte is used by the Hq/Hkv query heads of one group
 // and by nothing else, so the work is a stream over the cache at a few flops per byte: it is
-// bound by HBM bandwidth, not by math. It therefore runs on the CUDA cores, and the design goal
-// is to read each K/V byte exactly once with enough bytes in flight to keep HBM busy.
+// bound by HBM bandwidth, not by math. This kernel runs it on the CUDA cores, reading each K/V
+// byte exactly once with enough bytes in flight to keep HBM busy. fa_paged_fwd sends decode
+// batches to the tensor-core kernel instead (prefill.cu: GQA packing and key splits), which
+// measured faster for every group; this kernel serves fa_paged_decode_noalloc and, with the
+// environment variable FA_DECODE_TC=0, fa_paged_fwd's decode batches of groups 1, 2, 4 and 8.
 //
 // Grid: (split, sequence, kv-head block). A CTA streams 16-row blocks of its sequence's pages
 // (one page when page_size = 16) through a ring of shared-memory stages filled by bulk async
-// copies, one warp per kv head; lane 0 of warp 0 refills a stage as soon as all warps release it. Each warp keeps its group's query heads in registers, computes
-// the scores of 16 rows, updates the running max m and sum l once per block, and accumulates
-// O += p v. A CTA writes one partial state per (split, query head): O normalised over its keys
-// and its LSE; the last CTA of a sequence to finish merges the splits (with one split the CTA
-// writes the final O and LSE itself).
+// copies, one warp per kv head; lane 0 of warp 0 refills a stage as soon as all warps release
+// it. Each warp keeps its group's query heads in registers, computes the scores of 16 rows,
+// updates the running max m and sum l once per block, and accumulates O += p v. A CTA writes
+// one partial state per (split, query head): O normalised over its keys and its LSE; the last
+// CTA of a sequence to finish merges the splits (with one split the CTA writes the final O and
+// LSE itself).
 #include <cuda_bf16.h>
 #include "kernels.cuh"
 

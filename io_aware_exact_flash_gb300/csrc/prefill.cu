@@ -6,6 +6,9 @@
 //
 // One kernel serves the dense layout and the paged/ragged layout of the page's section
 // "FlashInfer: I/O-aware attention for serving"; they differ only in how tiles are addressed.
+// On the paged layout it also packs the query heads of a GQA group into one tile (rows = token x
+// head) and can split each unit's keys into ranges written as fp32 partial states, which makes it
+// the path for prefill, chunked prefill, multi-token verify and decode alike.
 //
 // CTA organisation (384 threads, one CTA per SM):
 //   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into a ring of stages
