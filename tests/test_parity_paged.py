@@ -225,3 +225,25 @@ def test_mixed_and_verify_workloads_full_size(name):
     compare(bf16_to_f64(o[ridx[:, 0], ridx[:, 1]]), o_ref, lse[ridx[:, 0], ridx[:, 1]].cpu().numpy(), lse_ref,
             f"{name} full size")
     assert bool(torch.isfinite(o.float()).all())
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_many_tiny_sequences(decode):
+    """1500 sequences of 0 to 40 keys: many work items, many packed tiles with a few rows, empty
+    sequences among them, and (decode) an automatic split plan over very short key ranges."""
+    rng = np.random.default_rng(81 + decode)
+    lengths = rng.integers(0, 41, size=1500).tolist()
+    t = build_case(lengths, 32, 8, 128, 16, decode, 83 + decode, extra_pages=2)
+    o, lse = run_paged(t, True, 1 / math.sqrt(128))
+    o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(128))
+    compare(o, o_ref, lse, lse_ref, f"1500 tiny sequences decode={decode}")
+
+
+def test_decode_more_splits_than_key_tiles():
+    """An explicit split count far above the key tiles of most sequences: most splits are empty
+    (LSE = -inf) and must drop out of the merge."""
+    lengths = [1, 17, 130, 700, 2000]
+    t = build_case(lengths, 32, 8, 128, 16, True, 91)
+    o, lse = run_paged(t, True, 1 / math.sqrt(128), num_splits=64)
+    o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(128))
+    compare(o, o_ref, lse, lse_ref, "decode with 64 splits")
