@@ -14,13 +14,18 @@ pytestmark = pytest.mark.gpu
 NAN_BF16 = np.uint16(0x7FC0)
 
 
-def build_case(lengths, Hq, Hkv, d, page_size, decode, seed, q_lens=None, extra_pages=0, poison=True):
+def build_case(lengths, Hq, Hkv, d, page_size, decode, seed, q_lens=None, extra_pages=0, poison=True, v_half=False):
     """Paged inputs for the given kv lengths (q_len = kv_len for prefill, 1 for decode, or
     explicit q_lens). Unused slots of last pages and `extra_pages` unreferenced pool pages hold
-    NaN when poison is set, so any read of them would show in the output."""
+    NaN when poison is set, so any read of them would show in the output. v_half halves V
+    (exactly, in bf16), which keeps |O| below 2 where rows attend to very few keys."""
     w = PagedWorkload("case", num_seqs=len(lengths), len_lo=0, len_hi=0, Hq=Hq, Hkv=Hkv, d=d,
                       page_size=page_size, causal=True, decode=decode, seed=seed, lengths=list(lengths))
     t = make_paged(w)
+    if v_half:
+        from io_aware_exact_flash_gb300.workloads import bf16_bits, bits_to_f32
+
+        t["v_pages"] = bf16_bits(bits_to_f32(t["v_pages"]) * np.float32(0.5))
     if q_lens is not None:
         from io_aware_exact_flash_gb300.workloads import normal_bf16
 
@@ -230,10 +235,13 @@ def test_mixed_and_verify_workloads_full_size(name):
 @pytest.mark.parametrize("decode", [False, True])
 def test_many_tiny_sequences(decode):
     """1500 sequences of 0 to 40 keys: many work items, many packed tiles with a few rows, empty
-    sequences among them, and (decode) an automatic split plan over very short key ranges."""
+    sequences among them, and (decode) an automatic split plan over very short key ranges. Rows
+    with a handful of keys can reach |O| of 2 to 4 with N(0,1) values, where bf16 P and the bf16
+    output together can exceed the 1e-2 bound by themselves; V is halved so that bound keeps its
+    margin and the test checks the planning and addressing it is here for."""
     rng = np.random.default_rng(81 + decode)
     lengths = rng.integers(0, 41, size=1500).tolist()
-    t = build_case(lengths, 32, 8, 128, 16, decode, 83 + decode, extra_pages=2)
+    t = build_case(lengths, 32, 8, 128, 16, decode, 83 + decode, extra_pages=2, v_half=True)
     o, lse = run_paged(t, True, 1 / math.sqrt(128))
     o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(128))
     compare(o, o_ref, lse, lse_ref, f"1500 tiny sequences decode={decode}")
