@@ -255,3 +255,19 @@ def test_decode_more_splits_than_key_tiles():
     o, lse = run_paged(t, True, 1 / math.sqrt(128), num_splits=64)
     o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(128))
     compare(o, o_ref, lse, lse_ref, "decode with 64 splits")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4)])
+def test_more_query_rows_than_keys(Hq, Hkv):
+    """Sequences with more query rows than keys: under bottom-right causal masking their top
+    q_len - kv_len rows see no key (O = 0, LSE = -inf); without masking every row sees them all."""
+    kv = [20, 10, 100, 0, 64]
+    q = [50, 10, 300, 7, 65]
+    t = build_case(kv, Hq, Hkv, 128, 16, False, 97 + Hq, q_lens=q)
+    for causal in (True, False):
+        o, lse = run_paged(t, causal, 0.1)
+        o_ref, lse_ref = oracle_paged(t, causal, 0.1)
+        compare(o, o_ref, lse, lse_ref, f"q_len > kv_len causal={causal}")
+        if causal:
+            top = np.isneginf(lse_ref)
+            assert top.any() and np.all(o[top] == 0)
