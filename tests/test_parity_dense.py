@@ -155,3 +155,26 @@ def test_full_size_sampled_rows(name, n_random):
     compare(bf16_to_f64(o_s), o_ref, l_s.cpu().numpy(), lse_ref, name)
     # properties that hold at any size: every row finite, LSE finite
     assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
+
+
+def test_dense_long_sequence_sampled():
+    """B=1, S=131072, GQA 2 (causal): query rows and key positions far from zero on the dense
+    path, checked on sampled rows (tile edges, the last rows, random rows)."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    B, S, Hq, Hkv, d = 1, 131072, 2, 1, 128
+    q = normal_bf16(111, (B, S, Hq, d), stream=0)
+    k = normal_bf16(111, (B, S, Hkv, d), stream=1)
+    v = normal_bf16(111, (B, S, Hkv, d), stream=2)
+    o, lse = fa.fa_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True, scale=1 / math.sqrt(d))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    idx = np.concatenate([[0, 127, 128, 255, 256, S - 129, S - 128, S - 1], rng.integers(0, S, 24)])
+    rows = np.stack([np.zeros_like(idx), idx, rng.integers(0, Hq, len(idx))], axis=1).astype(np.int64)
+    o_ref, lse_ref = oracle.get().dense_rows(q, k, v, True, 1 / math.sqrt(d), rows)
+    ridx = torch.from_numpy(rows).cuda()
+    compare(bf16_to_f64(o[ridx[:, 0], ridx[:, 1], ridx[:, 2]]), o_ref,
+            lse[ridx[:, 0], ridx[:, 1], ridx[:, 2]].cpu().numpy(), lse_ref, "dense S=131072")
+

@@ -271,3 +271,26 @@ def test_more_query_rows_than_keys(Hq, Hkv):
         if causal:
             top = np.isneginf(lse_ref)
             assert top.any() and np.all(o[top] == 0)
+
+
+def test_decode_one_million_keys():
+    """Decode at a million cached keys (MQA: 8 query heads on one kv head, so the pool stays
+    ~0.5 GB): page ids and key positions far from zero, hundreds of key splits, one large merge.
+    Every output row against the oracle."""
+    lengths = [1_000_000, 3]
+    t = build_case(lengths, 8, 1, 128, 16, True, 101, poison=False)
+    o, lse = run_paged(t, True, 1 / math.sqrt(128))
+    o_ref, lse_ref = oracle_paged(t, True, 1 / math.sqrt(128))
+    compare(o, o_ref, lse, lse_ref, "decode at 1M keys")
+
+
+def test_chunk_deep_in_a_long_context():
+    """Chunked prefill of 300 new tokens behind 200,000 cached keys (bottom-right causal), next
+    to a short sequence: large key-tile indices on the tensor-core path."""
+    lengths = [200_300, 50]
+    t = build_case(lengths, 8, 2, 128, 16, False, 103, q_lens=[300, 50], poison=False)
+    o, lse = run_paged(t, True, 1 / math.sqrt(128))
+    rows = np.array([[0, 0], [1, 3], [150, 5], [299, 7], [300, 1], [349, 6]], np.int64)
+    o_ref, lse_ref = oracle.get().paged_rows(t["q"], t["k_pages"], t["v_pages"], t["page_table"], t["cu_seqlens_q"],
+                                             t["kv_lens"], True, 1 / math.sqrt(128), rows)
+    compare(o[rows[:, 0], rows[:, 1]], o_ref, lse[rows[:, 0], rows[:, 1]], lse_ref, "chunk at 200K keys")
