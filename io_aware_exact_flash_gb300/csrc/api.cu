@@ -111,8 +111,6 @@ struct DecodePlan {
   int heads_per_cta;
 };
 
-int blocks_of_pages(int pages, int page_size) { return pages * (page_size / 16); }
-
 DecodePlan plan_decode(int num_seqs, int page_size, int max_pages_per_seq, int num_pages, int Hkv, int num_splits,
                        int sm_count) {
   DecodePlan d;
