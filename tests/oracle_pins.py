@@ -34,8 +34,9 @@ def _close(a, b, tol, what):
     both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
     with np.errstate(invalid="ignore"):
         err = np.where(both_inf, 0.0, np.abs(a - b))
-    worst = float(np.nanmax(err)) if err.size else 0.0
-    assert not np.isnan(err).any() and worst <= tol, f"{what}: max error {worst} > {tol}"
+    assert not np.isnan(err).any(), f"{what}: NaN where a finite value or a matching infinity was expected"
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= tol, f"{what}: max error {worst} > {tol}"
 
 
 # ------------------------------------------------------------------------- closed forms
