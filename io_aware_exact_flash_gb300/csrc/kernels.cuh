@@ -102,7 +102,8 @@ inline void decode_scratch_layout(void* base, int splits, int num_seqs, int Hq, 
 int current_device_info(DeviceStatus** status, int* sm_count);
 
 // Launchers (return cudaGetLastError() of the launch)
-// Prefill launches are persistent: min(units, sm_count) CTAs loop over the work units.
+// Dense prefill launches one CTA per work item (a CTA that finishes takes over the items of CTAs
+// that have not started); paged prefill is persistent: min(units, sm_count) CTAs loop over units.
 cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cudaStream_t stream);
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
                                  int2* work_list, int* work_count, cudaStream_t stream);

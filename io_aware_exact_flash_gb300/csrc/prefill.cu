@@ -10,6 +10,10 @@
 // head) and can split each unit's keys into ranges written as fp32 partial states, which makes it
 // the path for prefill, chunked prefill, multi-token verify and decode alike.
 //
+// The grid has one CTA per work item, and a CTA that finishes its item takes over the item of a
+// CTA that has not started yet (cluster launch control), so an SM pays the CTA set-up once while
+// items still run in the launch order the units are numbered in.
+//
 // CTA organisation (384 threads, one CTA per SM):
 //   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into a ring of stages
 //   warp 1      TMEM owner; one lane issues every tcgen05.mma of query tile 0
@@ -59,6 +63,7 @@ enum : uint32_t {
   kSiteSoftmaxO = 6,
   kSiteDrain = 7,
   kSiteMmaTurn = 8,
+  kSiteTakeOver = 9,
 };
 
 // One unit of work: a pair of 128-row query tiles of one (sequence, query head), or, with GQA
@@ -219,35 +224,81 @@ __device__ __forceinline__ int unit_of_round(int r) {
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-// Paired schedule (dense causal): CTA c takes two units of one query head, query-tile pair i
-// and its mirror T-1-i, heaviest first. Under causal masking every pair then costs the same, so
-// the hardware scheduler balances CTAs well, half as many CTAs start, and the second unit's
-// prologue overlaps the first unit's tail. Returns a unit index of the dense order (unit_at), or
-// n_units when the CTA has no unit for this round.
+// Work items of the dense launches: one unit, or under causal masking a mirrored pair of units —
+// query-tile pair i and its mirror T-1-i of one query head, heaviest first. Every pair then costs
+// the same, so CTAs stay balanced. Returns unit `sub` of item `item` as an index of the dense
+// order (unit_at), or -1 when the item has no such unit.
 template <bool PAGED>
-__device__ __forceinline__ int unit_of_pair_round(const PrefillParams& p, int r, int n_units) {
+__device__ __forceinline__ int item_unit(const PrefillParams& p, int item, int sub, int n_units) {
+  if (!p.pair_units) return sub == 0 && item < n_units ? item : -1;
   if constexpr (PAGED) {
-    return n_units;
+    return -1;
   } else {
     const int T = (p.S + 2 * kBM - 1) / (2 * kBM);
     const int half = (T + 1) / 2;  // pairs per query head
     const int G = p.group;
     const int NKV = p.B * p.Hkv;
     const int pairs_per_chunk = p.kv_heads_per_chunk * G * half;
-    const int c = blockIdx.x;
-    const int chunk = c / pairs_per_chunk;
+    const int chunk = item / pairs_per_chunk;
     const int kv0 = chunk * p.kv_heads_per_chunk;
     const int width = min(p.kv_heads_per_chunk, NKV - kv0) * G;
-    const int rc = c - chunk * pairs_per_chunk;
+    const int rc = item - chunk * pairs_per_chunk;
     const int i = rc / width, head = rc % width;
     const int chunk_start = chunk * p.kv_heads_per_chunk * G * T;
-    if (r == 0) return chunk_start + i * width + head;                              // qt2 = T-1-i
-    if (r == 1 && T - 1 - i != i) return chunk_start + (T - 1 - i) * width + head;  // qt2 = i
-    return n_units;
+    if (sub == 0) return chunk_start + i * width + head;                              // qt2 = T-1-i
+    if (sub == 1 && T - 1 - i != i) return chunk_start + (T - 1 - i) * width + head;  // qt2 = i
+    return -1;
   }
 }
 
-template <int D, bool PAGED>
+// Launch cancellation state shared by the warps that walk the units: two response slots, each
+// with a full barrier (the response's 16 bytes) and an empty barrier (one arrival per walker).
+struct TakeOver {
+  uint4 resp[2];
+  uint64_t full[2], empty[2];
+};
+constexpr int kUnitWalkers = 11;  // warps 0-2 and 4-11
+
+// Which units a CTA runs, in the same sequence in every warp. A persistent launch walks the snake
+// order of unit_of_round. Otherwise a CTA runs work item blockIdx.x; with TAKE, once its item is
+// done it takes over the item of a CTA that has not started yet: the producer requests a launch
+// cancellation while it loads the item's last unit, and every walker reads the response. CTAs then run items in the hardware's launch order (which keeps the
+// L2-aware unit order) while a CTA's set-up — barriers, TMEM, the first loads — is paid once per
+// SM rather than once per item, and the next item's first loads overlap this item's tail.
+struct Cursor {
+  int item, sub;   // current item and its next unit
+  uint32_t taken;  // responses read so far
+};
+
+template <bool PAGED, bool TAKE>
+__device__ __forceinline__ int next_unit(const PrefillParams& p, Cursor& c, int r, int n_units, TakeOver& t,
+                                         volatile int* abort) {
+  if constexpr (!TAKE) {
+    if (p.pair_units) return r < 2 ? item_unit<PAGED>(p, blockIdx.x, r, n_units) : -1;
+    const int u = unit_of_round(r);
+    return u < n_units ? u : -1;
+  }
+  for (;;) {
+    if (c.sub < 2) {
+      const int u = item_unit<PAGED>(p, c.item, c.sub++, n_units);
+      if (u >= 0) return u;
+      continue;
+    }
+    const uint32_t s = c.taken & 1, parity = (c.taken >> 1) & 1;
+    ++c.taken;
+    int item = -1;
+    if (mbar_wait(&t.full[s], parity, abort, p.status, kSiteTakeOver)) item = launch_cancel_result(&t.resp[s]);
+    item = __shfl_sync(0xffffffffu, item, 0);  // lane 0 decides for its warp
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&t.empty[s]);
+    // A failed request, or an item without units (a grid that is an upper bound ends with such
+    // items), ends the walk: the producer asks for another item only after loading a unit.
+    if (item < 0 || item_unit<PAGED>(p, item, 0, n_units) < 0) return -1;
+    c.item = item;
+    c.sub = 0;
+  }
+}
+
+template <int D, bool PAGED, bool TAKE>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
   constexpr int NS = C::kStages;
@@ -261,6 +312,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_full[NS], bar_empty[NS];
   __shared__ uint64_t bar_s[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_o_free[kQTiles], bar_drain[kQTiles];
   __shared__ uint64_t bar_turn[2];
+  __shared__ alignas(16) TakeOver take;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -286,6 +338,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     for (int g = 0; g < kQTiles; ++g) mbar_init(&bar_drain[g], 1);
     mbar_init(&bar_turn[0], 1);
     mbar_init(&bar_turn[1], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&take.full[s], 1);
+      mbar_init(&take.empty[s], kUnitWalkers);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -309,9 +365,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const uint64_t kv_policy = policy_evict_last();
     const uint64_t q_policy = policy_evict_first();
     uint32_t kv_it = 0;  // position in the K/V ring, continued across units
+    Cursor cur{(int)blockIdx.x, 0, 0u};
+    uint32_t requests = 0;  // launch cancellations requested
     for (int r = 0;; ++r) {
-      const int u = p.pair_units ? unit_of_pair_round<PAGED>(p, r, n_units) : unit_of_round(r);
-      if (u >= n_units) break;
+      const int u = next_unit<PAGED, TAKE>(p, cur, r, n_units, take, abort);
+      if (u < 0) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
       if (lane == 0) {
@@ -376,7 +434,30 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         }
         __syncwarp();
       }
+      // The item's last unit is loaded: ask for the next item now, about a ring's depth of key
+      // tiles before the walkers need it. One request is in flight at a time, and none follows a
+      // failed one (the walk ends there).
+      if (TAKE && item_unit<PAGED>(p, cur.item, cur.sub, n_units) < 0) {
+        int issued = 0;
+        if (lane == 0 && !*abort) {
+          const uint32_t s = requests & 1;  // the slot's previous response must have been read
+          if (requests < 2 || mbar_wait(&take.empty[s], ((requests >> 1) + 1) & 1, abort, p.status, kSiteTakeOver)) {
+            fence_proxy_async_smem();  // the walkers' reads of the slot precede the new response
+            mbar_arrive_expect_tx(&take.full[s], 16);
+            launch_cancel_request(&take.resp[s], &take.full[s]);
+            issued = 1;
+          }
+        }
+        requests += __shfl_sync(0xffffffffu, issued, 0);
+      }
     }
+    // After an abort the walk may end before the last response arrived: wait for it (bounded)
+    // so that nothing is written to this CTA's shared memory after it exits.
+    if (TAKE && lane == 0 && *abort && requests > 0) {
+      int no_abort = 0;
+      mbar_wait(&take.full[(requests - 1) & 1], ((requests - 1) >> 1) & 1, &no_abort, p.status, kSiteTakeOver);
+    }
+    __syncwarp();
   } else if (warp == 1 || warp == 2) {
     regs_dec<kRegsControl>();
     // ================================================================ MMA issuers
@@ -413,9 +494,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       mbar_arrive(&bar_turn[1 - g]);
       ++turn;
     };
+    Cursor cur{(int)blockIdx.x, 0, 0u};
     for (int r = 0;; ++r) {
-      const int u = p.pair_units ? unit_of_pair_round<PAGED>(p, r, n_units) : unit_of_round(r);
-      if (u >= n_units) break;
+      const int u = next_unit<PAGED, TAKE>(p, cur, r, n_units, take, abort);
+      if (u < 0) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
       const int nkv = g == 0 ? w.nkv[0] : w.nkv[1];
@@ -529,9 +611,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const uint32_t tO = tmem + C::kColO + g * D + lane_off;
     const float sl2 = p.scale_log2;
     uint32_t tcnt = 0, ounits = 0;
+    Cursor cur{(int)blockIdx.x, 0, 0u};
     for (int r = 0;; ++r) {
-      const int u = p.pair_units ? unit_of_pair_round<PAGED>(p, r, n_units) : unit_of_round(r);
-      if (u >= n_units) break;
+      const int u = next_unit<PAGED, TAKE>(p, cur, r, n_units, take, abort);
+      if (u < 0) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
       const int nkv = g == 0 ? w.nkv[0] : w.nkv[1];
@@ -706,23 +789,29 @@ __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t*
   }
 }
 
-// Grid size. Dense causal: one CTA per pair of mirrored query-tile pairs (unit_of_pair_round);
-// dense non-causal: one CTA per unit. The hardware scheduler hands CTAs to SMs as they free up,
-// which measured faster than a persistent static order for dense work. Paged: one CTA per SM
-// looping over units in the snake order (measured faster there). The environment variable
-// FA_PREFILL_PERSISTENT=0 (one CTA per unit) or 1 (persistent) overrides both.
+// Grid size: one CTA per work item — dense causal, two mirrored query-tile pairs (item_unit);
+// otherwise one unit — and a CTA that finishes takes over a pending CTA's item (next_unit)
+// instead of exiting. Items then run in the hardware's launch order, the order the units are
+// numbered in for L2 reuse, which measured faster than a persistent grid with a static order.
+// FA_PREFILL_TAKE_OVER=0 turns the take-over off: dense CTAs then exit after their own item and
+// paged work runs on a persistent grid (one CTA per SM, snake order). FA_PREFILL_PERSISTENT=0
+// (one CTA per unit, no take-over) or 1 (persistent) overrides both.
+int env_mode(const char* name) {
+  const char* e = getenv(name);
+  return (e == nullptr || (e[0] != '0' && e[0] != '1')) ? -1 : (e[0] == '1');  // -1: not set
+}
 int persistent_override() {
-  static int mode = -2;
-  if (mode == -2) {
-    const char* e = getenv("FA_PREFILL_PERSISTENT");
-    mode = (e == nullptr || (e[0] != '0' && e[0] != '1')) ? -1 : (e[0] == '1');
-  }
-  return mode;  // -1: no override
+  static const int mode = env_mode("FA_PREFILL_PERSISTENT");
+  return mode;
+}
+int take_over_enabled() {
+  static const int mode = env_mode("FA_PREFILL_TAKE_OVER");
+  return mode != 0;
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool TAKE = false>
 cudaError_t launch_prefill_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
-  auto kern = prefill_kernel<D, PAGED>;
+  auto kern = prefill_kernel<D, PAGED, TAKE>;
   {
     // The register split (kRegsControl / kRegsSoftmax) draws on the registers the CTA launches
     // with; a larger split would make the increase wait forever, so refuse to launch instead.
@@ -753,20 +842,23 @@ cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cu
   const int n2 = (p.S + 2 * kBM - 1) / (2 * kBM);
   const long long units = (long long)n2 * p.B * p.Hq;
   const int mode = persistent_override();
+  PrefillParams q = p;
   int grid;
+  bool take = false;
   if (mode == 1) {
     grid = (int)(units < sm_count ? units : sm_count);
   } else if (mode == 0 || !p.causal) {
     grid = (int)units;
+    take = mode != 0 && take_over_enabled();
   } else {
-    PrefillParams q = p;  // causal: mirrored query-tile pairs, one pair per CTA
-    q.pair_units = 1;
+    q.pair_units = 1;  // causal: mirrored query-tile pairs, one pair per work item
+    take = take_over_enabled();
     grid = ((n2 + 1) / 2) * p.B * p.Hq;
-    if (d == 128) return launch_prefill_impl<128, false>(q, grid, stream);
-    return launch_prefill_impl<64, false>(q, grid, stream);
   }
-  if (d == 128) return launch_prefill_impl<128, false>(p, grid, stream);
-  return launch_prefill_impl<64, false>(p, grid, stream);
+  if (d == 128) {
+    return take ? launch_prefill_impl<128, false, true>(q, grid, stream) : launch_prefill_impl<128, false>(q, grid, stream);
+  }
+  return take ? launch_prefill_impl<64, false, true>(q, grid, stream) : launch_prefill_impl<64, false>(q, grid, stream);
 }
 
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
@@ -778,10 +870,14 @@ cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, in
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long units = (long long)max_items * (p.Hq / p.pack) * p.kv_splits;
-  const bool persistent = persistent_override() != 0;
+  const int mode = persistent_override();
+  const bool take = mode == -1 && take_over_enabled();
+  const bool persistent = mode == 1 || (mode == -1 && !take);
   const int grid = (int)((units < sm_count || !persistent) ? units : sm_count);
-  if (d == 128) return launch_prefill_impl<128, true>(p, grid, stream);
-  return launch_prefill_impl<64, true>(p, grid, stream);
+  if (d == 128) {
+    return take ? launch_prefill_impl<128, true, true>(p, grid, stream) : launch_prefill_impl<128, true>(p, grid, stream);
+  }
+  return take ? launch_prefill_impl<64, true, true>(p, grid, stream) : launch_prefill_impl<64, true>(p, grid, stream);
 }
 
 }  // namespace fa

@@ -107,6 +107,32 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------- launch cancellation -----------------------------------
+// Cluster launch control (sm_100 and later): ask the hardware to cancel the launch of a CTA of
+// this grid that has not started yet. The 16-byte response lands in `resp` (16-byte aligned
+// shared memory) and completes 16 transaction bytes on `bar`, like a TMA load. A CTA must not ask
+// again after it has seen a request fail.
+__device__ __forceinline__ void launch_cancel_request(void* resp, uint64_t* bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(smem_u32(resp)), "r"(smem_u32(bar))
+               : "memory");
+}
+// Decode a response: the x index of the cancelled CTA, or -1 when the request failed (every CTA
+// of the grid has started).
+__device__ __forceinline__ int launch_cancel_result(const void* resp) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(smem_u32(resp))
+      : "memory");
+  return ok ? (int)x : -1;
+}
+
 // ---------------------------------- TMA ---------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -39,6 +39,10 @@ CASES = [
     (1, 2048, 2, 2, 128, True),
     (2, 2048, 16, 16, 128, True),  # head chunks of the persistent schedule, the last one partial
     (1, 1024, 24, 8, 64, False),   # several rounds of the persistent schedule, GQA 3
+    # more work items than SMs: CTAs that finish take over the items of CTAs not yet started
+    (1, 512, 320, 64, 64, True),   # 320 mirrored-pair items, GQA 5
+    (1, 300, 160, 32, 128, True),  # 160 items with a ragged tail
+    (1, 256, 304, 304, 64, False), # 304 one-unit items
 ]
 
 
@@ -178,3 +182,47 @@ def test_dense_long_sequence_sampled():
     compare(bf16_to_f64(o[ridx[:, 0], ridx[:, 1], ridx[:, 2]]), o_ref,
             lse[ridx[:, 0], ridx[:, 1], ridx[:, 2]].cpu().numpy(), lse_ref, "dense S=131072")
 
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,causal", [
+    (4, 4096, 32, 32, True),    # the causal prefill workload's shape: many more work items than SMs
+    (4, 4096, 32, 32, False),
+    (1, 32768, 32, 8, True),    # the long-context GQA workload's shape
+])
+def test_full_size_every_row_closed_form(B, S, Hq, Hkv, causal):
+    """Every output row of a full-size launch, against a closed form. All keys of a (batch, kv
+    head) are one row k and all its values one constant c, so every allowed score of row i is
+    equal: O = c exactly and LSE = scale * q_i . k + ln(n_i), n_i the number of allowed keys.
+    O and LSE start as NaN, so a work item that no CTA ran, or a row written with another head's
+    data, fails here whichever rows a sampled check would have picked."""
+    import torch
+
+    import io_aware_exact_flash_gb300 as fa
+
+    d = 128
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(d)
+    q = normal_bf16(321, (B, S, Hq, d), stream=0)
+    krow = normal_bf16(321, (B, 1, Hkv, d), stream=1)
+    k = np.ascontiguousarray(np.broadcast_to(krow, (B, S, Hkv, d)))
+    c = (1 + np.arange(B * Hkv) % 64).reshape(B, Hkv) / 16.0   # exact in bf16
+    c_bits = c.astype(np.float32).view(np.uint32) >> np.uint32(16)
+    v = np.ascontiguousarray(np.broadcast_to(c_bits.astype(np.uint16)[:, None, :, None], (B, S, Hkv, d)))
+    out = torch.full((B, S, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, S, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal, scale=scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == (0, 0)
+    c_dev = torch.from_numpy(np.repeat(c, G, axis=1)).cuda()  # (B, Hq)
+    o_err = (out.double() - c_dev[:, None, :, None]).abs().amax().item()
+    assert o_err <= 1e-2, f"max |O - c| = {o_err}"
+    qf = (q.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    kf = (krow.astype(np.uint32) << np.uint32(16)).view(np.float32)[:, 0]  # (B, Hkv, d)
+    n = np.arange(1, S + 1, dtype=np.float64) if causal else np.full(S, float(S))
+    lse_gpu = lse.cpu().numpy().astype(np.float64)
+    worst = 0.0
+    for b in range(B):
+        for h in range(Hq):
+            s = qf[b, :, h, :].astype(np.float64) @ kf[b, h // G].astype(np.float64)
+            worst = max(worst, float(np.abs(lse_gpu[b, :, h] - (scale * s + np.log(n))).max()))
+    assert worst <= 1e-3, f"max |dLSE| = {worst}"
