@@ -277,24 +277,25 @@ __device__ __forceinline__ int next_unit(const PrefillParams& p, Cursor& c, int 
     if (p.pair_units) return r < 2 ? item_unit<PAGED>(p, blockIdx.x, r, n_units) : -1;
     const int u = unit_of_round(r);
     return u < n_units ? u : -1;
-  }
-  for (;;) {
-    if (c.sub < 2) {
-      const int u = item_unit<PAGED>(p, c.item, c.sub++, n_units);
-      if (u >= 0) return u;
-      continue;
+  } else {
+    for (;;) {
+      if (c.sub < 2) {
+        const int u = item_unit<PAGED>(p, c.item, c.sub++, n_units);
+        if (u >= 0) return u;
+        continue;
+      }
+      const uint32_t s = c.taken & 1, parity = (c.taken >> 1) & 1;
+      ++c.taken;
+      int item = -1;
+      if (mbar_wait(&t.full[s], parity, abort, p.status, kSiteTakeOver)) item = launch_cancel_result(&t.resp[s]);
+      item = __shfl_sync(0xffffffffu, item, 0);  // lane 0 decides for its warp
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&t.empty[s]);
+      // A failed request, or an item without units (a grid that is an upper bound ends with such
+      // items), ends the walk: the producer asks for another item only after loading a unit.
+      if (item < 0 || item_unit<PAGED>(p, item, 0, n_units) < 0) return -1;
+      c.item = item;
+      c.sub = 0;
     }
-    const uint32_t s = c.taken & 1, parity = (c.taken >> 1) & 1;
-    ++c.taken;
-    int item = -1;
-    if (mbar_wait(&t.full[s], parity, abort, p.status, kSiteTakeOver)) item = launch_cancel_result(&t.resp[s]);
-    item = __shfl_sync(0xffffffffu, item, 0);  // lane 0 decides for its warp
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&t.empty[s]);
-    // A failed request, or an item without units (a grid that is an upper bound ends with such
-    // items), ends the walk: the producer asks for another item only after loading a unit.
-    if (item < 0 || item_unit<PAGED>(p, item, 0, n_units) < 0) return -1;
-    c.item = item;
-    c.sub = 0;
   }
 }
 
