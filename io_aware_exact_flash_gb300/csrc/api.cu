@@ -248,8 +248,14 @@ bool decode_on_tensor_cores(int group) {
 // (small decode batches, one long shared prefix); each split keeps at least 8 key tiles, and
 // the partial states are kept under 1 GiB. (Targets of 2, 3, 4 and 6 waves with at least 4 or 8
 // tiles were measured on decode batches of 4 to 64 sequences and the cascade; 3 and 8 was best
-// or level everywhere.) requested > 0 fixes the count (capped at the key
-// tiles of the longest sequence).
+// or level everywhere.) Units whose two query tiles are full (a shared prefix seen by many query
+// rows) are compute bound instead, and there whole waves matter: the count with the shortest
+// estimated makespan, waves x (key tiles per split + a per-unit cost of kSplitUnitCostTiles key
+// tiles: loads, epilogue, partial state), is taken. On the cascade's prefix (16 units over 128
+// key tiles) that is 9 splits, one wave, 60 us, against 16 splits, 1.7 waves, 73 us (the per-unit
+// cost was fitted to a sweep of 4 to 24 splits there). requested > 0 fixes the count (capped at
+// the key tiles of the longest sequence).
+constexpr int kSplitUnitCostTiles = 6;
 int plan_kv_splits(int num_seqs, int total_q, int max_q_len, int pack, int Hq, int d, int max_kv_tiles,
                    int sm_count, int requested) {
   if (max_kv_tiles < 1) max_kv_tiles = 1;
@@ -261,10 +267,26 @@ int plan_kv_splits(int num_seqs, int total_q, int max_q_len, int pack, int Hq, i
   const long long units = items * (Hq / pack);
   const long long target = 3LL * sm_count;
   if (units <= 0 || units >= target) return 1;
-  long long s = (target + units - 1) / units;
-  if (s > max_kv_tiles / 8) s = max_kv_tiles / 8;
+  long long s_max = max_kv_tiles / 8;
   const long long part = (long long)total_q * Hq * (d + 1) * 4;
-  if (part > 0 && s * part > (1LL << 30)) s = (1LL << 30) / part;
+  if (part > 0 && s_max * part > (1LL << 30)) s_max = (1LL << 30) / part;
+  if (s_max < 1) return 1;
+  long long s;
+  if ((long long)max_q_len * pack >= 2 * fa::kBM) {
+    s = 1;
+    long long best = -1;
+    for (long long c = 1; c <= s_max; ++c) {
+      const long long waves = (units * c + sm_count - 1) / sm_count;
+      const long long cost = waves * ((max_kv_tiles + c - 1) / c + kSplitUnitCostTiles);
+      if (best < 0 || cost < best) {
+        best = cost;
+        s = c;
+      }
+    }
+  } else {
+    s = (target + units - 1) / units;
+    if (s > s_max) s = s_max;
+  }
   return s < 1 ? 1 : (int)s;
 }
 
