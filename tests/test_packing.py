@@ -1,7 +1,8 @@
 """Path choices of the entry points, forced each way for the parity suites (their smaller cases),
 so every shape there is checked against the oracle on each path: GQA packing of the tensor-core
 path (a tile's rows = token x head of one kv head's query heads) on and off, decode batches on the
-split-KV CUDA-core kernel instead of the tensor cores, and the prefill launch modes."""
+split-KV CUDA-core kernel instead of the tensor cores, and the prefill launch modes. The seeded
+random shapes of test_fuzz.py run under each of them too."""
 import os
 import subprocess
 import sys
@@ -17,7 +18,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
                          ids=["always_pack", "never_pack", "decode_on_cuda_cores"])
 def test_paged_parity_with_forced_paths(env):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-k", "not full_size",
-                        "-p", "no:cacheprovider", "tests/test_parity_paged.py", "tests/test_cascade.py"],
+                        "-p", "no:cacheprovider", "tests/test_parity_paged.py", "tests/test_cascade.py",
+                        "tests/test_fuzz.py"],
                        env=dict(os.environ, **env), cwd=ROOT, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
 
@@ -28,9 +30,9 @@ def test_paged_parity_with_forced_paths(env):
 def test_launch_modes(env):
     """The prefill launch modes other than the default take-over: dense CTAs that exit after their
     own item with a persistent paged grid, a persistent grid everywhere, and one CTA per unit.
-    Each runs the dense, paged and cascade parity suites (their smaller cases)."""
+    Each runs the dense, paged, cascade and random-shape parity suites (their smaller cases)."""
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-k", "not full_size",
                         "-p", "no:cacheprovider", "tests/test_parity_dense.py", "tests/test_parity_paged.py",
-                        "tests/test_cascade.py"],
+                        "tests/test_cascade.py", "tests/test_fuzz.py"],
                        env=dict(os.environ, **env), cwd=ROOT, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
