@@ -1,13 +1,15 @@
 """Thin Python binding over the C ABI in ``include/fa.h`` (library ``libfa_gb300.so``).
 
 Every function here only marshals arguments: it checks tensor dtypes, devices and shapes,
-allocates outputs with torch when the caller passes none, and forwards raw device pointers and
-the current CUDA stream to the C entry point of the same name. All attention arithmetic runs in
+allocates outputs with torch when the caller passes none (on the stream the call runs on), and
+forwards raw device pointers and the given (or current) CUDA stream to the C entry point of the
+same name. All attention arithmetic runs in
 the library's sm_103a kernels; there is no other path. If the library is missing, loading fails
 with an error that says so.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -99,6 +101,13 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _on(stream):
+    """Tensors a call allocates (outputs, workspace) belong to the stream the call runs on, so
+    the caching allocator does not hand their memory to other work while the call's kernels
+    still use it (a workspace is released as soon as the call returns)."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 def _bf16_cuda(name, t, dim):
     if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
@@ -123,10 +132,11 @@ def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=Tru
     if k.shape != (B, S, Hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, S, Hkv, d] matching q")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, S, Hq), dtype=torch.float32, device=q.device)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty((B, S, Hq), dtype=torch.float32, device=q.device)
     lib = load_library()
     code = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, d, int(bool(causal)), scale,
                       _stream(stream))
@@ -168,14 +178,15 @@ def fa_paged_fwd(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, max_q_l
     if dk != d or v_pages.shape != k_pages.shape:
         raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
     need = fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages, num_pages, Hq, Hkv, d,
                                     num_splits)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lib = load_library()
     code = lib.fa_paged_fwd(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(cu_seqlens_q),
@@ -195,10 +206,11 @@ def fa_merge_states(o_parts, lse_parts, out=None, lse=None, return_lse=True, str
     P, n, H, d = o_parts.shape
     if lse_parts.shape != (P, n, H):
         raise ValueError("lse_parts must be [P, n, H]")
-    if out is None:
-        out = torch.empty((n, H, d), dtype=torch.bfloat16, device=o_parts.device)
-    if lse is None and return_lse:
-        lse = torch.empty((n, H), dtype=torch.float32, device=o_parts.device)
+    with _on(stream):
+        if out is None:
+            out = torch.empty((n, H, d), dtype=torch.bfloat16, device=o_parts.device)
+        if lse is None and return_lse:
+            lse = torch.empty((n, H), dtype=torch.float32, device=o_parts.device)
     code = load_library().fa_merge_states(_ptr(o_parts), _ptr(lse_parts), P, n, H, d, _ptr(out), _ptr(lse),
                                           _stream(stream))
     _check("fa_merge_states", code)
@@ -229,15 +241,16 @@ def fa_cascade_fwd(q, k_pages, v_pages, cu_q_groups, prefix_page_table, prefix_l
     if cu_q_groups.shape != (num_groups + 1,) or prefix_lens.shape != (num_groups,):
         raise ValueError("cu_q_groups must be [num_groups + 1] and prefix_lens [num_groups]")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
     lib = load_library()
     need = lib.fa_cascade_workspace_bytes(num_groups, num_seqs, total_q, int(max_group_q_len), int(max_q_len),
                                           page_size, max_prefix_pages, max_pages, num_pages, Hq, Hkv, d)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     code = lib.fa_cascade_fwd(_ptr(q), _ptr(k_pages), _ptr(v_pages), page_size, num_pages, Hq, Hkv, d, scale,
                               num_groups, _ptr(cu_q_groups), _ptr(prefix_page_table), _ptr(prefix_lens),

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include "../../include/fa.h"
 #include "kernels.cuh"
@@ -207,12 +208,14 @@ fa_status check_paged_shape(int num_seqs, int total_q, int max_q_len, int page_s
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Reads a 0/1 switch from the environment once; -1 when it is unset or holds anything else.
-int env_switch(const char* name, int* cache) {
-  if (*cache == -2) {
+int env_switch(const char* name, std::atomic<int>* cache) {
+  int v = cache->load(std::memory_order_relaxed);
+  if (v == -2) {
     const char* e = getenv(name);
-    *cache = (e == nullptr || (e[0] != '0' && e[0] != '1') || e[1] != '\0') ? -1 : (e[0] == '1');
+    v = (e == nullptr || (e[0] != '0' && e[0] != '1') || e[1] != '\0') ? -1 : (e[0] == '1');
+    cache->store(v, std::memory_order_relaxed);
   }
-  return *cache;
+  return v;
 }
 
 bool pow2_group(int group) { return group >= 2 && group <= fa::kBM && (group & (group - 1)) == 0; }
@@ -226,7 +229,7 @@ bool pow2_group(int group) { return group >= 2 && group <= fa::kBM && (group & (
 int choose_pack(int group, int max_q_len) {
   (void)max_q_len;
   if (!pow2_group(group)) return 1;
-  static int mode = -2;
+  static std::atomic<int> mode{-2};
   return env_switch("FA_PAGED_PACK", &mode) == 0 ? 1 : group;
 }
 
@@ -237,7 +240,7 @@ int choose_pack(int group, int max_q_len) {
 // row per tile), 32 sequences 5501 vs 4501. FA_DECODE_TC=0 sends groups 1, 2, 4 and 8 (the
 // groups that kernel takes) to the CUDA-core kernel.
 bool decode_on_tensor_cores(int group) {
-  static int mode = -2;
+  static std::atomic<int> mode{-2};
   if (group == 1 || group == 2 || group == 4 || group == 8) return env_switch("FA_DECODE_TC", &mode) != 0;
   return true;
 }

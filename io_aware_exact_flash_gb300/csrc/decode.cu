@@ -19,6 +19,7 @@
 // CTA of a sequence to finish merges the splits (with one split the CTA writes the final O and
 // LSE itself).
 #include <cuda_bf16.h>
+#include <atomic>
 #include "kernels.cuh"
 
 namespace fa {
@@ -402,13 +403,18 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
   int n_stages = (200 * 1024) / (2 * chunk);
   n_stages = max(2, min(8, n_stages));
   const int smem = 128 + n_stages * 2 * chunk;
-  static int configured_smem[32] = {0};  // largest dynamic smem already allowed, per device
+  // largest dynamic smem already allowed, per device (atomics: calls may come from several threads)
+  static std::atomic<int> configured_smem[32];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 32 || configured_smem[dev] < smem) {
+  if (dev >= 32 || configured_smem[dev].load(std::memory_order_acquire) < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev < 32) configured_smem[dev] = smem;
+    if (dev < 32) {
+      int seen = configured_smem[dev].load(std::memory_order_relaxed);
+      while (seen < smem && !configured_smem[dev].compare_exchange_weak(seen, smem, std::memory_order_release)) {
+      }
+    }
   }
   dim3 grid(p.num_splits, p.num_seqs, p.Hkv / p.heads_per_cta);
   if (p.num_splits > 1) {

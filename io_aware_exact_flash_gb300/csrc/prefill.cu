@@ -27,6 +27,7 @@
 // TMEM columns: S/P of tile g at [128 g, 128 g + 128) (P, as packed bf16 pairs, overwrites the
 // first 64 columns of S), O of tile g at [256 + g D, 256 + (g+1) D).
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cstdlib>
 #include "kernels.cuh"
 
@@ -816,22 +817,25 @@ cudaError_t launch_prefill_impl(const PrefillParams& p, int grid, cudaStream_t s
   {
     // The register split (kRegsControl / kRegsSoftmax) draws on the registers the CTA launches
     // with; a larger split would make the increase wait forever, so refuse to launch instead.
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
+    // (The caches below are atomics: calls may come from several host threads at once.)
+    static std::atomic<int> launch_regs{-1};
+    int regs = launch_regs.load(std::memory_order_relaxed);
+    if (regs < 0) {
       cudaFuncAttributes attr;
       const cudaError_t e = cudaFuncGetAttributes(&attr, kern);
       if (e != cudaSuccess) return e;
-      launch_regs = attr.numRegs;
+      regs = attr.numRegs;
+      launch_regs.store(regs, std::memory_order_relaxed);
     }
-    if (128 * kRegsControl + 256 * kRegsSoftmax > kPrefillThreads * launch_regs) return cudaErrorInvalidConfiguration;
+    if (128 * kRegsControl + 256 * kRegsSoftmax > kPrefillThreads * regs) return cudaErrorInvalidConfiguration;
   }
-  static int configured_mask = 0;  // one bit per device ordinal below 32
+  static std::atomic<unsigned> configured_mask{0u};  // one bit per device ordinal below 32
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 32 || !(configured_mask & (1 << dev))) {
+  if (dev >= 32 || !(configured_mask.load(std::memory_order_acquire) & (1u << dev))) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 32) configured_mask |= (1 << dev);
+    if (dev < 32) configured_mask.fetch_or(1u << dev, std::memory_order_release);
   }
   kern<<<grid, kPrefillThreads, Cfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
