@@ -26,6 +26,8 @@
  *  - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
  *    FA_OK means validated and enqueued. Calls on different streams may run concurrently as
  *    long as they do not share an output or a workspace.
+ *  - Threads: calls may be made from several host threads at once (with the exception noted at
+ *    fa_paged_decode_noalloc); the library's host-side caches are atomic or behind a mutex.
  *  - Errors: arguments are checked on the host before anything is enqueued; no exception ever
  *    crosses this boundary. Kernels never trap: a device-side wait that runs past its time limit
  *    sets the device status word, which fa_get_device_status reports.
