@@ -102,8 +102,9 @@ inline void decode_scratch_layout(void* base, int splits, int num_seqs, int Hq, 
 int current_device_info(DeviceStatus** status, int* sm_count);
 
 // Launchers (return cudaGetLastError() of the launch)
-// Dense prefill launches one CTA per work item (a CTA that finishes takes over the items of CTAs
-// that have not started); paged prefill is persistent: min(units, sm_count) CTAs loop over units.
+// Prefill launches have one CTA per work item, and a CTA that finishes takes over the items of CTAs
+// that have not started; with the take-over off, paged work runs on a persistent grid instead
+// (min(units, sm_count) CTAs looping over the units).
 cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cudaStream_t stream);
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
                                  int2* work_list, int* work_count, cudaStream_t stream);
