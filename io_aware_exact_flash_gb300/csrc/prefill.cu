@@ -743,22 +743,101 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 // Work list for the paged prefill: one item per (sequence, pair of query tiles). Sequences come
 // longest first (a counting sort on their key-tile count); the items of one sequence are
 // contiguous, heaviest query tiles first, so the CTAs running together share one sequence's
-// K/V pages in L2 while the order still starts with the longest work.
+// K/V pages in L2 while the order still starts with the longest work. With at most one sequence
+// per thread the sort is done in parallel: each thread counts the sequences that go before its
+// own (longer, or as long with a lower index), and a block scan gives the item offsets. Larger
+// batches run the sort's serial steps (bucket offsets, stable placement, item offsets) in one
+// thread; up to kPlanStagedSeqs sequences their inputs are first copied to shared memory by all
+// threads, so each serial step waits on shared memory rather than on an L2 load.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanStagedSeqs = 4096;
+
 __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ kv_lens,
                                   int num_seqs, int causal, int pack, int max_cost, int max_items,
                                   int2* __restrict__ work_list, int* __restrict__ work_count,
                                   int* __restrict__ order) {
-  extern __shared__ int hist[];  // max_cost + 1 buckets
+  extern __shared__ int plan_smem[];
+  int* hist = plan_smem;  // max_cost + 1 buckets
+  const bool staged = num_seqs <= kPlanStagedSeqs;
+  int* s_cost = hist + max_cost + 1;  // staged: [num_seqs] key-tile cost of each sequence
+  int* s_items = s_cost + num_seqs;   // staged: [num_seqs] items (tile pairs) of each sequence
+  int* s_order = s_items + num_seqs;  // staged: [2 num_seqs] the order and each one's first item
   const int tid = threadIdx.x, nt = blockDim.x;
   __shared__ int total;
-  for (int c = tid; c <= max_cost; c += nt) hist[c] = 0;
-  __syncthreads();
-  auto cost_of = [&](int s) {
+  auto cost_in = [&](int s) {
     const int kv = kv_lens[s];
     return min(kv > 0 ? (kv + kBN - 1) / kBN : 0, max_cost);
   };
-  for (int s = tid; s < num_seqs; s += nt) atomicAdd(&hist[cost_of(s)], 1);
+  auto items_in = [&](int s) {
+    const int q_len = cu[s + 1] - cu[s];
+    return q_len > 0 ? (q_len * pack + 2 * kBM - 1) / (2 * kBM) : 0;
+  };
+  if (num_seqs <= nt) {
+    // one sequence per thread: rank = sequences that sort before this one
+    const int my_cost = tid < num_seqs ? cost_in(tid) : -1;
+    const int my_items = tid < num_seqs ? items_in(tid) : 0;
+    if (tid < num_seqs) s_cost[tid] = my_cost;
+    __syncthreads();
+    int rank = 0;
+    if (tid < num_seqs)
+      for (int j = 0; j < num_seqs; ++j) {
+        const int c = s_cost[j];
+        rank += (c > my_cost) | ((c == my_cost) & (j < tid));
+      }
+    if (tid < num_seqs) {
+      s_order[rank] = tid;
+      s_items[rank] = my_items;  // items in sorted position
+    }
+    __syncthreads();
+    // exclusive scan of the sorted item counts: warp scans, then a scan of the warp totals
+    const int lane = tid & 31, wid = tid >> 5;
+    const int v = tid < num_seqs ? s_items[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __shared__ int warp_sum[kPlanThreads / 32];
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int w = lane < nt / 32 ? warp_sum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive scan of the warp totals
+    }
+    __syncthreads();
+    const int base = incl - v + (wid > 0 ? warp_sum[wid - 1] : 0);
+    if (tid == nt - 1) {
+      total = min(base + v, max_items);  // more items than the host bound means inconsistent lengths
+      *work_count = total;
+    }
+    __syncthreads();
+    if (tid < num_seqs) {
+      const int s = s_order[tid];
+      for (int it = 0; it < v; ++it) {
+        const int pos = base + it;
+        if (pos < total) work_list[pos] = make_int2(s, causal ? v - 1 - it : it);
+      }
+    }
+    return;
+  }
+  for (int c = tid; c <= max_cost; c += nt) hist[c] = 0;
   __syncthreads();
+  for (int s = tid; s < num_seqs; s += nt) {
+    const int c = cost_in(s);
+    if (staged) {
+      s_cost[s] = c;
+      s_items[s] = items_in(s);
+    }
+    atomicAdd(&hist[c], 1);
+  }
+  __syncthreads();
+  int* ord = staged ? s_order : order;
   if (tid == 0) {
     // bucket offsets, longest first; then a stable placement of every sequence, then item offsets
     int run = 0;
@@ -767,23 +846,21 @@ __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t*
       hist[c] = run;
       run += t;
     }
-    for (int s = 0; s < num_seqs; ++s) order[hist[cost_of(s)]++] = s;
+    for (int s = 0; s < num_seqs; ++s) ord[hist[staged ? s_cost[s] : cost_in(s)]++] = s;
     int items = 0;
     for (int k = 0; k < num_seqs; ++k) {
-      const int s = order[k];
-      const int q_len = cu[s + 1] - cu[s];
-      order[num_seqs + k] = items;  // first item of the k-th sequence in the order
-      items += q_len > 0 ? (q_len * pack + 2 * kBM - 1) / (2 * kBM) : 0;
+      const int s = ord[k];
+      ord[num_seqs + k] = items;  // first item of the k-th sequence in the order
+      items += staged ? s_items[s] : items_in(s);
     }
     total = min(items, max_items);  // more items than the host bound means inconsistent lengths
     *work_count = total;
   }
   __syncthreads();
   for (int k = tid; k < num_seqs; k += nt) {
-    const int s = order[k];
-    const int q_len = cu[s + 1] - cu[s];
-    const int n = q_len > 0 ? (q_len * pack + 2 * kBM - 1) / (2 * kBM) : 0;
-    const int base = order[num_seqs + k];
+    const int s = ord[k];
+    const int n = staged ? s_items[s] : items_in(s);
+    const int base = ord[num_seqs + k];
     for (int it = 0; it < n; ++it) {
       const int pos = base + it;
       if (pos < total) work_list[pos] = make_int2(s, causal ? n - 1 - it : it);
@@ -868,9 +945,22 @@ cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cu
 
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
                                  int2* work_list, int* work_count, cudaStream_t stream) {
-  const int smem = (max_kv_tiles + 1) * (int)sizeof(int);
+  const int staged = p.num_seqs <= kPlanStagedSeqs ? 4 * p.num_seqs : 0;  // ints staged per sort
+  const int smem = (max_kv_tiles + 1 + staged) * (int)sizeof(int);
+  {
+    // up to (8192 + 1 + 4 * 4096) ints = 98 KB: above the default dynamic shared memory limit
+    constexpr int kPlanSmemMax = (8192 + 1 + 4 * kPlanStagedSeqs) * (int)sizeof(int);
+    static std::atomic<unsigned> configured_mask{0u};  // one bit per device ordinal below 32
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 32 || !(configured_mask.load(std::memory_order_acquire) & (1u << dev))) {
+      cudaError_t e = cudaFuncSetAttribute(plan_paged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
+      if (e != cudaSuccess) return e;
+      if (dev < 32) configured_mask.fetch_or(1u << dev, std::memory_order_release);
+    }
+  }
   int* order = reinterpret_cast<int*>(work_list + max_items);  // 2 * num_seqs ints of scratch
-  plan_paged_kernel<<<1, 1024, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, p.pack,
+  plan_paged_kernel<<<1, kPlanThreads, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, p.pack,
                                               max_kv_tiles, max_items, work_list, work_count, order);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

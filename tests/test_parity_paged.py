@@ -247,6 +247,18 @@ def test_many_tiny_sequences(decode):
     compare(o, o_ref, lse, lse_ref, f"1500 tiny sequences decode={decode}")
 
 
+def test_more_sequences_than_the_planner_stages():
+    """5000 sequences (prefill chunks of 1 to 6 rows over 0 to 300 keys): more than the work-list
+    planner copies to shared memory, so its serial sort reads lengths from device memory."""
+    rng = np.random.default_rng(85)
+    lengths = rng.integers(0, 301, size=5000).tolist()
+    q_lens = [min(L, int(rng.integers(1, 7))) for L in lengths]
+    t = build_case(lengths, 8, 2, 64, 16, False, 87, q_lens=q_lens, v_half=True)
+    o, lse = run_paged(t, True, 0.125)
+    o_ref, lse_ref = oracle_paged(t, True, 0.125)
+    compare(o, o_ref, lse, lse_ref, "5000 sequences")
+
+
 def test_decode_more_splits_than_key_tiles():
     """An explicit split count far above the key tiles of most sequences: most splits are empty
     (LSE = -inf) and must drop out of the merge."""
