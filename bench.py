@@ -55,8 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on (the
 # digest of its sources without comments); the bench reports it as roofline.traffic only while
 # that code is unchanged.
-PREFILL_TRAFFIC = {"bytes": 431814912 + 112332800,
-                   "source_sha256": "53e938a3756caf03bfd7e3f1e83298ce47e300535395c575b5ec0e438de85d6e"}
+PREFILL_TRAFFIC = {"bytes": 429601536 + 112393728,
+                   "source_sha256": "a3de4d96b47ce48dbabc3c7fd38303f2ccf71da2fe5d6fcf40c406e73e79f839"}
 L2_FLUSH_BYTES = 512 << 20
 
 
