@@ -741,29 +741,51 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 }
 
 // Work list for the paged prefill: one item per (sequence, pair of query tiles). Sequences come
-// longest first (a counting sort on their key-tile count); the items of one sequence are
-// contiguous, heaviest query tiles first, so the CTAs running together share one sequence's
-// K/V pages in L2 while the order still starts with the longest work. With at most one sequence
-// per thread the sort is done in parallel: each thread counts the sequences that go before its
-// own (longer, or as long with a lower index), and a block scan gives the item offsets. Larger
-// batches run the sort's serial steps (bucket offsets, stable placement, item offsets) in one
-// thread; up to kPlanStagedSeqs sequences their inputs are first copied to shared memory by all
-// threads, so each serial step waits on shared memory rather than on an L2 load.
+// longest first (a stable counting sort on their key-tile count); the items of one sequence are
+// contiguous, heaviest query tiles first, so the CTAs running together share one sequence's K/V
+// pages in L2 while the order still starts with the longest work. One CTA does it, in parallel:
+// with at most one sequence per thread each thread counts the sequences that sort before its own;
+// larger batches take a histogram of the counts, a scan of the buckets (longest first), a stable
+// placement in chunks of one sequence per thread (warps of a chunk in turn, so equal counts keep
+// their index order), and a scan of the item counts in the sorted order.
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanStagedSeqs = 4096;
 
-__global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ kv_lens,
-                                  int num_seqs, int causal, int pack, int max_cost, int max_items,
-                                  int2* __restrict__ work_list, int* __restrict__ work_count,
-                                  int* __restrict__ order) {
-  extern __shared__ int plan_smem[];
-  int* hist = plan_smem;  // max_cost + 1 buckets
-  const bool staged = num_seqs <= kPlanStagedSeqs;
-  int* s_cost = hist + max_cost + 1;  // staged: [num_seqs] key-tile cost of each sequence
-  int* s_items = s_cost + num_seqs;   // staged: [num_seqs] items (tile pairs) of each sequence
-  int* s_order = s_items + num_seqs;  // staged: [2 num_seqs] the order and each one's first item
-  const int tid = threadIdx.x, nt = blockDim.x;
+// Exclusive scan across the block of one int per thread; returns this thread's prefix and leaves
+// the block total in *total_out. Uses warp_sums[32] of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total_out) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive scan of the warp totals
+  }
+  __syncthreads();
+  const int excl = incl - v + (wid > 0 ? warp_sums[wid - 1] : 0);
+  *total_out = warp_sums[nw - 1];
+  __syncthreads();  // warp_sums may be reused by the next scan
+  return excl;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_paged_kernel(
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ kv_lens, int num_seqs, int causal, int pack,
+    int max_cost, int max_items, int2* __restrict__ work_list, int* __restrict__ work_count,
+    int* __restrict__ scratch) {
+  extern __shared__ int plan_smem[];  // max_cost + 1 buckets, or (<= nt sequences) 2 * nt ints
+  __shared__ int warp_sums[32];
   __shared__ int total;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5;
   auto cost_in = [&](int s) {
     const int kv = kv_lens[s];
     return min(kv > 0 ? (kv + kBN - 1) / kBN : 0, max_cost);
@@ -772,99 +794,83 @@ __global__ void plan_paged_kernel(const int32_t* __restrict__ cu, const int32_t*
     const int q_len = cu[s + 1] - cu[s];
     return q_len > 0 ? (q_len * pack + 2 * kBM - 1) / (2 * kBM) : 0;
   };
+  // order[k]: the k-th sequence of the sorted order
+  int* order = num_seqs <= nt ? plan_smem + nt : scratch;
   if (num_seqs <= nt) {
     // one sequence per thread: rank = sequences that sort before this one
+    int* s_cost = plan_smem;
     const int my_cost = tid < num_seqs ? cost_in(tid) : -1;
-    const int my_items = tid < num_seqs ? items_in(tid) : 0;
     if (tid < num_seqs) s_cost[tid] = my_cost;
     __syncthreads();
-    int rank = 0;
-    if (tid < num_seqs)
+    if (tid < num_seqs) {
+      int rank = 0;
       for (int j = 0; j < num_seqs; ++j) {
         const int c = s_cost[j];
         rank += (c > my_cost) | ((c == my_cost) & (j < tid));
       }
-    if (tid < num_seqs) {
-      s_order[rank] = tid;
-      s_items[rank] = my_items;  // items in sorted position
+      order[rank] = tid;
     }
     __syncthreads();
-    // exclusive scan of the sorted item counts: warp scans, then a scan of the warp totals
-    const int lane = tid & 31, wid = tid >> 5;
-    const int v = tid < num_seqs ? s_items[tid] : 0;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    __shared__ int warp_sum[kPlanThreads / 32];
-    if (lane == 31) warp_sum[wid] = incl;
+  } else {
+    int* hist = plan_smem;  // per count: sequences, then the next free position of that count
+    for (int c = tid; c <= max_cost; c += nt) hist[c] = 0;
     __syncthreads();
-    if (wid == 0) {
-      int w = lane < nt / 32 ? warp_sum[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
+    for (int s = tid; s < num_seqs; s += nt) atomicAdd(&hist[cost_in(s)], 1);
+    __syncthreads();
+    // bucket starts, longest first: each thread scans a run of counts from the top down
+    const int per = (max_cost + 1 + nt - 1) / nt;
+    const int hi = max_cost - tid * per;  // this thread's counts: hi, hi-1, ..., hi-per+1 (>= 0)
+    int mine = 0;
+    for (int i = 0; i < per; ++i)
+      if (hi - i >= 0) mine += hist[hi - i];
+    int unused;
+    int run = block_exclusive_scan(mine, warp_sums, &unused);
+    for (int i = 0; i < per; ++i)
+      if (hi - i >= 0) {
+        const int t = hist[hi - i];
+        hist[hi - i] = run;
+        run += t;
       }
-      warp_sum[lane] = w;  // inclusive scan of the warp totals
-    }
     __syncthreads();
-    const int base = incl - v + (wid > 0 ? warp_sum[wid - 1] : 0);
-    if (tid == nt - 1) {
-      total = min(base + v, max_items);  // more items than the host bound means inconsistent lengths
-      *work_count = total;
-    }
-    __syncthreads();
-    if (tid < num_seqs) {
-      const int s = s_order[tid];
-      for (int it = 0; it < v; ++it) {
-        const int pos = base + it;
-        if (pos < total) work_list[pos] = make_int2(s, causal ? v - 1 - it : it);
+    // stable placement, one chunk of nt sequences at a time, the warps of a chunk in turn
+    for (int base = 0; base < num_seqs; base += nt) {
+      const int s = base + tid;
+      const int c = s < num_seqs ? cost_in(s) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, c);
+      const int leader = __ffs(peers) - 1;
+      const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+      for (int w = 0; w < nt / 32; ++w) {
+        if (wid == w && s < num_seqs && lane == leader) {
+          const int start = hist[c];
+          hist[c] = start + __popc(peers);
+          warp_sums[lane] = start;  // handed to the group below
+        }
+        __syncwarp();
+        if (wid == w && s < num_seqs) order[warp_sums[leader] + rank_in_warp] = s;
+        __syncthreads();
       }
     }
-    return;
   }
-  for (int c = tid; c <= max_cost; c += nt) hist[c] = 0;
-  __syncthreads();
-  for (int s = tid; s < num_seqs; s += nt) {
-    const int c = cost_in(s);
-    if (staged) {
-      s_cost[s] = c;
-      s_items[s] = items_in(s);
-    }
-    atomicAdd(&hist[c], 1);
-  }
-  __syncthreads();
-  int* ord = staged ? s_order : order;
+  // item offsets in the sorted order: each thread scans a run of consecutive positions
+  const int per = (num_seqs + nt - 1) / nt;
+  const int k0 = tid * per;
+  int mine = 0;
+  for (int i = 0; i < per && k0 + i < num_seqs; ++i) mine += items_in(order[k0 + i]);
+  int all_items;
+  int run = block_exclusive_scan(mine, warp_sums, &all_items);
   if (tid == 0) {
-    // bucket offsets, longest first; then a stable placement of every sequence, then item offsets
-    int run = 0;
-    for (int c = max_cost; c >= 0; --c) {
-      const int t = hist[c];
-      hist[c] = run;
-      run += t;
-    }
-    for (int s = 0; s < num_seqs; ++s) ord[hist[staged ? s_cost[s] : cost_in(s)]++] = s;
-    int items = 0;
-    for (int k = 0; k < num_seqs; ++k) {
-      const int s = ord[k];
-      ord[num_seqs + k] = items;  // first item of the k-th sequence in the order
-      items += staged ? s_items[s] : items_in(s);
-    }
-    total = min(items, max_items);  // more items than the host bound means inconsistent lengths
+    total = min(all_items, max_items);  // more items than the host bound means inconsistent lengths
     *work_count = total;
   }
   __syncthreads();
-  for (int k = tid; k < num_seqs; k += nt) {
-    const int s = ord[k];
-    const int n = staged ? s_items[s] : items_in(s);
-    const int base = ord[num_seqs + k];
+  for (int i = 0; i < per && k0 + i < num_seqs; ++i) {
+    const int s = order[k0 + i];
+    const int n = items_in(s);
     for (int it = 0; it < n; ++it) {
-      const int pos = base + it;
+      const int pos = run + it;
       if (pos < total) work_list[pos] = make_int2(s, causal ? n - 1 - it : it);
     }
+    run += n;
   }
 }
 
@@ -945,23 +951,12 @@ cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cu
 
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
                                  int2* work_list, int* work_count, cudaStream_t stream) {
-  const int staged = p.num_seqs <= kPlanStagedSeqs ? 4 * p.num_seqs : 0;  // ints staged per sort
-  const int smem = (max_kv_tiles + 1 + staged) * (int)sizeof(int);
-  {
-    // up to (8192 + 1 + 4 * 4096) ints = 98 KB: above the default dynamic shared memory limit
-    constexpr int kPlanSmemMax = (8192 + 1 + 4 * kPlanStagedSeqs) * (int)sizeof(int);
-    static std::atomic<unsigned> configured_mask{0u};  // one bit per device ordinal below 32
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 32 || !(configured_mask.load(std::memory_order_acquire) & (1u << dev))) {
-      cudaError_t e = cudaFuncSetAttribute(plan_paged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
-      if (e != cudaSuccess) return e;
-      if (dev < 32) configured_mask.fetch_or(1u << dev, std::memory_order_release);
-    }
-  }
-  int* order = reinterpret_cast<int*>(work_list + max_items);  // 2 * num_seqs ints of scratch
+  // buckets (at most 8193 ints), or for batches of at most one sequence per thread their counts
+  // and order (2 x 1024 ints): within the default dynamic shared memory limit either way
+  const int smem = (p.num_seqs <= kPlanThreads ? 2 * kPlanThreads : max_kv_tiles + 1) * (int)sizeof(int);
+  int* scratch = reinterpret_cast<int*>(work_list + max_items);  // 2 * num_seqs ints
   plan_paged_kernel<<<1, kPlanThreads, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, p.pack,
-                                              max_kv_tiles, max_items, work_list, work_count, order);
+                                                       max_kv_tiles, max_items, work_list, work_count, scratch);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long units = (long long)max_items * (p.Hq / p.pack) * p.kv_splits;

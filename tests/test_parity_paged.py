@@ -247,16 +247,18 @@ def test_many_tiny_sequences(decode):
     compare(o, o_ref, lse, lse_ref, f"1500 tiny sequences decode={decode}")
 
 
-def test_more_sequences_than_the_planner_stages():
-    """5000 sequences (prefill chunks of 1 to 6 rows over 0 to 300 keys): more than the work-list
-    planner copies to shared memory, so its serial sort reads lengths from device memory."""
-    rng = np.random.default_rng(85)
-    lengths = rng.integers(0, 301, size=5000).tolist()
+@pytest.mark.parametrize("n_seqs,max_len", [(5000, 300), (20000, 64)])
+def test_more_sequences_than_planner_threads(n_seqs, max_len):
+    """Thousands of sequences (prefill chunks of 1 to 6 rows over short, often equal lengths): more
+    than one per thread of the work-list planner, whose sort then runs over chunks of the batch
+    (a stable placement per chunk); every row must be planned exactly once."""
+    rng = np.random.default_rng(85 + n_seqs)
+    lengths = rng.integers(0, max_len + 1, size=n_seqs).tolist()
     q_lens = [min(L, int(rng.integers(1, 7))) for L in lengths]
     t = build_case(lengths, 8, 2, 64, 16, False, 87, q_lens=q_lens, v_half=True)
     o, lse = run_paged(t, True, 0.125)
     o_ref, lse_ref = oracle_paged(t, True, 0.125)
-    compare(o, o_ref, lse, lse_ref, "5000 sequences")
+    compare(o, o_ref, lse, lse_ref, f"{n_seqs} sequences")
 
 
 def test_decode_more_splits_than_key_tiles():
