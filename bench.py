@@ -55,8 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on (the
 # digest of its sources without comments); the bench reports it as roofline.traffic only while
 # that code is unchanged.
-PREFILL_TRAFFIC = {"bytes": 429601536 + 112393728,
-                   "source_sha256": "a3de4d96b47ce48dbabc3c7fd38303f2ccf71da2fe5d6fcf40c406e73e79f839"}
+PREFILL_TRAFFIC = {"bytes": 429091840 + 113318912,
+                   "source_sha256": "917b301208b2704c13aff043a4c119065699d7c7765b594da6a427078f7cbd1c"}
 L2_FLUSH_BYTES = 512 << 20
 
 
