@@ -161,3 +161,20 @@ def test_fa_paged_append_empty_rows_may_be_null(lib):
     # nothing to append: NULL row buffers pass validation (the call then needs a device)
     assert _append(lib, kn=0, vn=0, total_new=0) != 1
     assert _append(lib, kn=0, total_new=1) == 1
+
+
+def test_key_split_plan_is_host_only():
+    """The automatic key-split count (host planning, no GPU needed). A decode batch that fills
+    the GPU three times over is not split. A small decode batch is split with at least 8 key tiles
+    per split. A shared prefix read by 128 query rows (16 compute-bound units over 128 key tiles)
+    gets the count that fits one wave of this part's SMs, not the three-wave count."""
+    from io_aware_exact_flash_gb300 import binding
+
+    big_decode = binding.fa_paged_num_splits(128, 128, 1, 16, 1024, 70000, 32, 8, 128)
+    assert big_decode == 1
+    small_decode = binding.fa_paged_num_splits(4, 4, 1, 16, 1024, 70000, 32, 8, 128)
+    assert 2 <= small_decode <= (1024 * 16 // 128) // 8
+    prefix = binding.fa_paged_num_splits(1, 128, 128, 16, 1024, 70000, 32, 8, 128)
+    assert 2 <= prefix <= 16 and 16 * prefix <= 148  # one wave (148 or 152 SMs), each split >= 8 tiles
+    # no split when a pass has more units than three waves, whatever the key length
+    assert binding.fa_paged_num_splits(64, 64 * 512, 512, 16, 1024, 70000, 32, 8, 128) == 1
