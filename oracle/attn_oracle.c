@@ -13,7 +13,11 @@
  *
  * Every value is carried in fp64. Inputs arrive as bf16 bit patterns (uint16) and are widened
  * here, by this file's own conversion. Outputs are fp64: O and the natural-log LSE of the
- * scaled scores over the keys each row may attend to.
+ * scaled scores over the keys each row may attend to, and optionally, per element of O, the
+ * softmax-weighted mean magnitude of V, sum_j p_j |v_jc|. That quantity is not part of the
+ * method: the tests use it to bound, element by element, how far rounding the softmax weights to
+ * bf16 before P.V may move O (each weight moves by at most a relative 2^-8, so O_c moves by at
+ * most 2^-8 sum_j p_j |v_jc|).
  *
  * Readings where the pages are silent (each one is listed with its reason in the design notes):
  *  - causal masking is bottom-right aligned: query row i of a sequence with q_len rows and
@@ -44,12 +48,14 @@ static double bf16_to_double(uint16_t b) {
 
 /*
  * One query row against n_allowed keys (rows of K and V in fp64, row-major [n][d]).
- * s is caller scratch of at least n_allowed doubles.
+ * s is caller scratch of at least n_allowed doubles. vabs (d doubles) may be NULL.
  */
 static void attend_row(const double* q, const double* K, const double* V, long n_allowed, int d,
-                       double scale, double* s, double* o, double* lse) {
+                       double scale, double* s, double* o, double* lse, double* vabs) {
   if (n_allowed <= 0) {
     for (int c = 0; c < d; ++c) o[c] = 0.0;
+    if (vabs)
+      for (int c = 0; c < d; ++c) vabs[c] = 0.0;
     *lse = -INFINITY;
     return;
   }
@@ -76,6 +82,14 @@ static void attend_row(const double* q, const double* K, const double* V, long n
     for (int c = 0; c < d; ++c) o[c] += p * V[j * d + c];
   }
   *lse = m + log(sum);
+  /* mean magnitude of V under the same weights */
+  if (vabs) {
+    for (int c = 0; c < d; ++c) vabs[c] = 0.0;
+    for (long j = 0; j < n_allowed; ++j) {
+      double p = s[j] / sum;
+      for (int c = 0; c < d; ++c) vabs[c] += p * fabs(V[j * d + c]);
+    }
+  }
 }
 
 /* Number of keys query row i may attend to (bottom-right causal alignment). */
@@ -95,7 +109,7 @@ typedef struct {
   double scale;
   const int64_t* rows; /* n_rows triples (b, i, h) */
   int64_t n_rows;
-  double *o, *lse;
+  double *o, *lse, *vabs;
   int64_t begin, end;
   int status;
 } DenseJob;
@@ -124,7 +138,7 @@ static void* dense_worker(void* arg) {
         K[j * d + c] = bf16_to_double(J->k[at]);
         V[j * d + c] = bf16_to_double(J->v[at]);
       }
-    attend_row(qd, K, V, n, d, J->scale, s, J->o + r * d, J->lse + r);
+    attend_row(qd, K, V, n, d, J->scale, s, J->o + r * d, J->lse + r, J->vabs ? J->vabs + r * d : NULL);
   }
   free(qd); free(K); free(V); free(s);
   return NULL;
@@ -155,12 +169,13 @@ static int run_jobs(void* jobs, size_t job_size, int n_threads, void* (*fn)(void
 /*
  * Dense attention for selected query rows.
  *   q [B, Sq, Hq, d], k and v [B, Skv, Hkv, d]: bf16 bit patterns, contiguous.
- *   rows: n_rows triples (b, i, h); o [n_rows, d] and lse [n_rows]: fp64 outputs.
+ *   rows: n_rows triples (b, i, h); o [n_rows, d] and lse [n_rows]: fp64 outputs;
+ *   vabs [n_rows, d] or NULL.
  * Returns 0 on success, nonzero on bad arguments or allocation failure.
  */
 int oracle_dense_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int Sq, int Skv,
                       int Hq, int Hkv, int d, int causal, double scale, const int64_t* rows,
-                      int64_t n_rows, double* o, double* lse, int n_threads) {
+                      int64_t n_rows, double* o, double* lse, double* vabs, int n_threads) {
   if (B <= 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 2;
   for (int64_t r = 0; r < n_rows; ++r) {
     if (rows[3 * r] < 0 || rows[3 * r] >= B || rows[3 * r + 1] < 0 || rows[3 * r + 1] >= Sq ||
@@ -175,7 +190,7 @@ int oracle_dense_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
     DenseJob* J = &jobs[t];
     J->q = q; J->k = k; J->v = v;
     J->B = B; J->Sq = Sq; J->Skv = Skv; J->Hq = Hq; J->Hkv = Hkv; J->d = d; J->causal = causal;
-    J->scale = scale; J->rows = rows; J->n_rows = n_rows; J->o = o; J->lse = lse;
+    J->scale = scale; J->rows = rows; J->n_rows = n_rows; J->o = o; J->lse = lse; J->vabs = vabs;
     J->begin = n_rows * t / n_threads;
     J->end = n_rows * (t + 1) / n_threads;
   }
@@ -194,7 +209,7 @@ typedef struct {
   double scale;
   const int64_t* rows; /* n_rows pairs (token t, head h) */
   int64_t n_rows;
-  double *o, *lse;
+  double *o, *lse, *vabs;
   int64_t begin, end;
   int status;
 } PagedJob;
@@ -243,7 +258,7 @@ static void* paged_worker(void* arg) {
         V[j * d + c] = bf16_to_double(J->v_pages[at]);
       }
     }
-    attend_row(qd, K, V, n, d, J->scale, s, J->o + r * d, J->lse + r);
+    attend_row(qd, K, V, n, d, J->scale, s, J->o + r * d, J->lse + r, J->vabs ? J->vabs + r * d : NULL);
   }
   free(qd); free(K); free(V); free(s);
   return NULL;
@@ -253,13 +268,14 @@ static void* paged_worker(void* arg) {
  * Paged, ragged attention for selected (token, head) rows.
  *   q [total_q, Hq, d]; k_pages and v_pages [num_pages, page_size, Hkv, d] (bf16 bits);
  *   page_table [num_seqs, max_pages_per_seq] (int32, -1 = unused); cu_seqlens_q [num_seqs+1];
- *   kv_lens [num_seqs]; rows: n_rows pairs (t, h); o [n_rows, d], lse [n_rows] fp64.
+ *   kv_lens [num_seqs]; rows: n_rows pairs (t, h); o [n_rows, d], lse [n_rows] fp64;
+ *   vabs [n_rows, d] or NULL.
  */
 int oracle_paged_rows(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
                       const int32_t* page_table, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
                       int page_size, int num_seqs, int max_pages_per_seq, int num_pages, int Hq, int Hkv,
                       int d, int causal, double scale, const int64_t* rows, int64_t n_rows, double* o,
-                      double* lse, int n_threads) {
+                      double* lse, double* vabs, int n_threads) {
   if (page_size <= 0 || num_seqs <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 2;
   for (int s = 0; s < num_seqs; ++s) {
     if (kv_lens[s] < 0 || kv_lens[s] > (int64_t)max_pages_per_seq * page_size) return 2;
@@ -279,7 +295,7 @@ int oracle_paged_rows(const uint16_t* q, const uint16_t* k_pages, const uint16_t
     J->page_table = page_table; J->cu_seqlens_q = cu_seqlens_q; J->kv_lens = kv_lens;
     J->page_size = page_size; J->num_seqs = num_seqs; J->max_pages_per_seq = max_pages_per_seq;
     J->num_pages = num_pages; J->Hq = Hq; J->Hkv = Hkv; J->d = d; J->causal = causal;
-    J->scale = scale; J->rows = rows; J->n_rows = n_rows; J->o = o; J->lse = lse;
+    J->scale = scale; J->rows = rows; J->n_rows = n_rows; J->o = o; J->lse = lse; J->vabs = vabs;
     J->begin = n_rows * t / n_threads;
     J->end = n_rows * (t + 1) / n_threads;
   }

@@ -377,6 +377,55 @@ def pin_paged_rows_subset(orc):
     _close(l2, lse[rows[:, 0], rows[:, 1]], 0.0, "row subset LSE")
 
 
+def pin_vabs_closed_forms(orc):
+    """The softmax-weighted mean magnitude of V, sum_j p_j |v_jc|, in cases where the weights are
+    known in closed form. Identical keys: uniform weights over the n allowed keys, so it is the
+    mean of |v_jc| over those rows. Two keys whose scores differ by g: weights w = 1 / (1 + e^-g)
+    and 1 - w, so it is w |v_0c| + (1 - w) |v_1c|. Constant V = c: |c|. Dense and paged layouts;
+    a row with no key gives zero."""
+    rng = np.random.default_rng(31)
+    B, S, Hq, Hkv, d = 1, 12, 2, 1, 8
+    q = _bf(rng.standard_normal((B, S, Hq, d)))
+    k0 = _bf(rng.standard_normal((B, 1, Hkv, d)))
+    k = np.ascontiguousarray(np.broadcast_to(k0, (B, S, Hkv, d)))
+    v = _bf(rng.standard_normal((B, S, Hkv, d)) * 2.0)
+    vf = _f64(v)
+    _, _, va = orc.dense(q, k, v, True, 0.3, threads=2, vabs=True)
+    for i in range(S):
+        for h in range(Hq):
+            _close(va[0, i, h], np.abs(vf[0, :i + 1, 0]).mean(axis=0), 1e-13, "weighted |V| of identical keys")
+    # two keys with a known score gap: q = 2 e_0, k_0 = 1.5 e_0, k_1 = -0.25 e_0
+    d2 = 4
+    qq = np.zeros((1, 1, 1, d2), np.float32)
+    qq[0, 0, 0, 0] = 2.0
+    kk = np.zeros((1, 2, 1, d2), np.float32)
+    kk[0, 0, 0, 0], kk[0, 1, 0, 0] = 1.5, -0.25
+    vv = _bf(rng.standard_normal((1, 2, 1, d2)))
+    scale = 0.75
+    g = scale * 2.0 * (1.5 - (-0.25))
+    w = 1.0 / (1.0 + math.exp(-g))
+    vvf = _f64(vv)
+    _, _, va2 = orc.dense(_bf(qq), _bf(kk), vv, False, scale, threads=1, vabs=True)
+    _close(va2[0, 0, 0], w * np.abs(vvf[0, 0, 0]) + (1 - w) * np.abs(vvf[0, 1, 0]), 1e-13, "weighted |V| of two keys")
+    # constant V rows (negative, so the magnitude is taken)
+    vc = np.ascontiguousarray(np.broadcast_to(_bf(np.full((1, 1, Hkv, d), -1.75)), (B, S, Hkv, d)))
+    _, _, va3 = orc.dense(q, _bf(rng.standard_normal((B, S, Hkv, d))), vc, False, 0.3, threads=1, vabs=True)
+    _close(va3, np.full_like(va3, 1.75), 1e-13, "weighted |V| of constant V")
+    # paged: the identical-key case laid out in pages
+    pq, pk, pv, tab, cu, kv = _small_paged(32, [S], Hq, Hkv, d, 4, False)
+    pk = np.ascontiguousarray(np.broadcast_to(k0[0, 0][None, None], pk.shape))
+    _, _, vap = orc.paged(pq, pk, pv, tab, cu, kv, True, 0.3, threads=2, vabs=True)
+    vpf = _f64(pv)
+    seq_rows = np.stack([vpf[tab[0, j // 4], j % 4, 0] for j in range(S)])
+    for i in range(S):
+        _close(vap[i, 0], np.abs(seq_rows[:i + 1]).mean(axis=0), 1e-13, "paged weighted |V| of identical keys")
+    # a decode row of a sequence with no key has no weights: zero
+    pq, pk, pv, tab, cu, kv = _small_paged(33, [5, 0], Hq, Hkv, d, 4, True)
+    tab = np.where(tab < 0, 0, tab)  # the empty sequence's entry is never read
+    _, _, vae = orc.paged(pq, pk, pv, tab, cu, kv, True, 0.3, threads=1, vabs=True)
+    _close(vae[1], np.zeros_like(vae[1]), 0.0, "weighted |V| of a row with no key")
+
+
 ALL_PINS = [
     pin_identical_keys,
     pin_dominant_key,
@@ -394,4 +443,5 @@ ALL_PINS = [
     pin_bruteforce_high_precision,
     pin_paged_equals_dense,
     pin_paged_rows_subset,
+    pin_vabs_closed_forms,
 ]

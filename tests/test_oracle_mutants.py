@@ -22,6 +22,9 @@ MUTANTS = [
     ("wrong_page_slot", "const long slot = j % J->page_size;", "const long slot = (j + 1) % J->page_size;"),
     ("unnormalised_p", "double p = s[j] / sum;", "double p = s[j];"),
     ("max_not_updated", "if (s[j] > m) m = s[j];", "if (s[j] > m) m = m;"),
+    ("vabs_without_abs", "vabs[c] += p * fabs(V[j * d + c]);", "vabs[c] += p * V[j * d + c];"),
+    ("vabs_unweighted", "vabs[c] += p * fabs(V[j * d + c]);", "vabs[c] += fabs(V[j * d + c]);"),
+    ("vabs_centered_on_o", "vabs[c] += p * fabs(V[j * d + c]);", "vabs[c] += p * fabs(V[j * d + c] - o[c]);"),
 ]
 
 
