@@ -118,8 +118,8 @@ def test_append_then_decode():
                              max_q_len=1, causal=True, scale=1 / math.sqrt(d))
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == (0, 0)
-    o_ref, lse_ref = oracle.get().paged(q, ek, ev, c["table"], cu_q, kv_lens, True, 1 / math.sqrt(d))
-    compare(bf16_to_f64(o), o_ref, lse.cpu().numpy().astype(np.float64), lse_ref, "append then decode")
+    o_ref, lse_ref, va_ref = oracle.get().paged(q, ek, ev, c["table"], cu_q, kv_lens, True, 1 / math.sqrt(d), vabs=True)
+    compare(bf16_to_f64(o), o_ref, lse.cpu().numpy().astype(np.float64), lse_ref, "append then decode", vabs=va_ref)
 
 
 def test_append_full_size_prefill_batch():

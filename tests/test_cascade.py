@@ -74,7 +74,8 @@ def oracle_flat(c, causal, scale):
         k2[off:off + n].reshape(-1, *shape[2:])[:L] = rows_k[s]
         v2[off:off + n].reshape(-1, *shape[2:])[:L] = rows_v[s]
         off += n
-    return oracle.get().paged(c["q"], k2, v2, table2, c["cu"], np.asarray(lens, np.int32), causal, scale)
+    return oracle.get().paged(c["q"], k2, v2, table2, c["cu"], np.asarray(lens, np.int32), causal, scale,
+                              vabs=True)
 
 
 def run_cascade(c, causal, scale):
@@ -98,8 +99,8 @@ def test_cascade_decode_one_group(ps):
     c = build([len(suffix)], [300], [1] * len(suffix), suffix, 32, 8, 128, ps, seed=40 + ps)
     scale = 1 / math.sqrt(128)
     o, lse = run_cascade(c, True, scale)
-    o_ref, lse_ref = oracle_flat(c, True, scale)
-    compare(o, o_ref, lse, lse_ref, f"cascade decode ps={ps}")
+    o_ref, lse_ref, va_ref = oracle_flat(c, True, scale)
+    compare(o, o_ref, lse, lse_ref, f"cascade decode ps={ps}", vabs=va_ref)
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -114,8 +115,8 @@ def test_cascade_groups_and_chunks(causal, d, Hq, Hkv):
     c = build(groups, prefix, q_lens, suffix, Hq, Hkv, d, 16, seed=50 + d)
     scale = 1 / math.sqrt(d)
     o, lse = run_cascade(c, causal, scale)
-    o_ref, lse_ref = oracle_flat(c, causal, scale)
-    compare(o, o_ref, lse, lse_ref, f"cascade groups causal={causal} d={d}")
+    o_ref, lse_ref, va_ref = oracle_flat(c, causal, scale)
+    compare(o, o_ref, lse, lse_ref, f"cascade groups causal={causal} d={d}", vabs=va_ref)
 
 
 def test_cascade_full_size_decode():
@@ -134,6 +135,6 @@ def test_cascade_full_size_decode():
                                i32_dev(t["page_table"]), i32_dev(t["kv_lens"]), w.q_len, causal=True, scale=w.scale)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == (0, 0)
-    o_ref, lse_ref = oracle.get().paged(t["q"], t["k_pages"], t["v_pages"], t["flat_page_table"], t["cu_seqlens_q"],
-                                        t["flat_kv_lens"], True, w.scale)
-    compare(bf16_to_f64(o), o_ref, lse.cpu().numpy().astype(np.float64), lse_ref, "cascade full size")
+    o_ref, lse_ref, va_ref = oracle.get().paged(t["q"], t["k_pages"], t["v_pages"], t["flat_page_table"], t["cu_seqlens_q"],
+                                        t["flat_kv_lens"], True, w.scale, vabs=True)
+    compare(bf16_to_f64(o), o_ref, lse.cpu().numpy().astype(np.float64), lse_ref, "cascade full size", vabs=va_ref)

@@ -1,9 +1,9 @@
 """Seeded random shapes against the fp64 oracle: dense batches (lengths, head counts, GQA groups,
 head dims, masking, scales) and paged batches (ragged prefill, chunked prefill and decode rows,
 page sizes, groups that do and do not pack, forced and planned key splits, unused pool pages).
-Each case is drawn from its own seed, so a failure names a reproducible shape. V is halved
-(exactly, in bf16) so that rows with a handful of keys keep |O| < 2, where the 1e-2 bound has
-its margin above the bf16 output rounding."""
+Each case is drawn from its own seed, so a failure names a reproducible shape. Q, K and V are
+N(0,1), as in the workloads, so rows with a handful of keys (early causal rows, short sequences)
+reach |O| of 2 to 4, where the bf16 output rounding alone is 7.8e-3."""
 import math
 
 import numpy as np
@@ -15,13 +15,6 @@ from tests.helpers import bf16_to_f64, compare, to_dev
 from tests.test_parity_paged import build_case, oracle_paged, run_paged
 
 pytestmark = pytest.mark.gpu
-
-
-def _half_bits(bits):
-    """bf16 bit patterns of x / 2 (exact: only the exponent changes, inputs are normal N(0,1))."""
-    from io_aware_exact_flash_gb300.workloads import bf16_bits, bits_to_f32
-
-    return bf16_bits(bits_to_f32(bits) * np.float32(0.5))
 
 
 def dense_case(i):
@@ -45,13 +38,13 @@ def test_fuzz_dense(i):
     B, S, Hq, Hkv, d, causal, scale = dense_case(i)
     q = normal_bf16(6000 + i, (B, S, Hq, d), stream=0)
     k = normal_bf16(6000 + i, (B, S, Hkv, d), stream=1)
-    v = _half_bits(normal_bf16(6000 + i, (B, S, Hkv, d), stream=2))
+    v = normal_bf16(6000 + i, (B, S, Hkv, d), stream=2)
     o, lse = fa.fa_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal, scale=scale)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == (0, 0)
-    o_ref, lse_ref = oracle.get().dense(q, k, v, causal, scale)
+    o_ref, lse_ref, va_ref = oracle.get().dense(q, k, v, causal, scale, vabs=True)
     compare(bf16_to_f64(o), o_ref, lse.cpu().numpy().astype(np.float64), lse_ref,
-            f"dense case {i}: B={B} S={S} Hq={Hq} Hkv={Hkv} d={d} causal={causal} scale={scale:.3f}")
+            f"dense case {i}: B={B} S={S} Hq={Hq} Hkv={Hkv} d={d} causal={causal} scale={scale:.3f}", vabs=va_ref)
 
 
 def paged_case(i):
@@ -79,15 +72,14 @@ def paged_case(i):
 def test_fuzz_paged(i):
     kind, lengths, q_lens, Hq, Hkv, d, page_size, causal, splits, extra = paged_case(i)
     if kind == "decode":
-        t = build_case(lengths, Hq, Hkv, d, page_size, True, 8000 + i, extra_pages=extra, v_half=True)
+        t = build_case(lengths, Hq, Hkv, d, page_size, True, 8000 + i, extra_pages=extra)
     else:
-        t = build_case(lengths, Hq, Hkv, d, page_size, False, 8000 + i, q_lens=q_lens, extra_pages=extra,
-                       v_half=True)
+        t = build_case(lengths, Hq, Hkv, d, page_size, False, 8000 + i, q_lens=q_lens, extra_pages=extra)
     if int(t["q_lens"].sum()) == 0:
         pytest.skip("no query rows drawn")
     scale = 1 / math.sqrt(d)
     o, lse = run_paged(t, causal, scale, num_splits=splits)
-    o_ref, lse_ref = oracle_paged(t, causal, scale)
+    o_ref, lse_ref, va_ref = oracle_paged(t, causal, scale)
     compare(o, o_ref, lse, lse_ref,
             f"paged case {i}: {kind} lengths={lengths} q_lens={q_lens} Hq={Hq} Hkv={Hkv} d={d} "
-            f"page={page_size} causal={causal} splits={splits}")
+            f"page={page_size} causal={causal} splits={splits}", vabs=va_ref)

@@ -54,8 +54,8 @@ def test_dense_matches_oracle(B, S, Hq, Hkv, d, causal):
     v = normal_bf16(seed, (B, S, Hkv, d), stream=2)
     scale = 1.0 / math.sqrt(d)
     o, lse = run_fa(q, k, v, causal, scale)
-    o_ref, lse_ref = oracle.get().dense(q, k, v, causal, scale)
-    compare(o, o_ref, lse, lse_ref, f"dense {B, S, Hq, Hkv, d, causal}")
+    o_ref, lse_ref, va_ref = oracle.get().dense(q, k, v, causal, scale, vabs=True)
+    compare(o, o_ref, lse, lse_ref, f"dense {B, S, Hq, Hkv, d, causal}", vabs=va_ref)
 
 
 @pytest.mark.parametrize("gain", [4.0, 16.0])
@@ -69,12 +69,11 @@ def test_dense_large_scores_force_rescales(gain):
     q = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32) * gain)
     ramp = np.linspace(0.2, 2.0, S, dtype=np.float32)[None, :, None, None]
     k = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32) * ramp * gain)
-    # V is kept small so |O| < 2 and bf16 output rounding (half an ulp) stays below 4e-3
-    v = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32) * 0.25)
+    v = bf16_bits(rng.standard_normal((B, S, H, d)).astype(np.float32))
     for causal in (False, True):
         o, lse = run_fa(q, k, v, causal, 1.0 / math.sqrt(d))
-        o_ref, lse_ref = oracle.get().dense(q, k, v, causal, 1.0 / math.sqrt(d))
-        compare(o, o_ref, lse, lse_ref, f"large scores gain={gain} causal={causal}")
+        o_ref, lse_ref, va_ref = oracle.get().dense(q, k, v, causal, 1.0 / math.sqrt(d), vabs=True)
+        compare(o, o_ref, lse, lse_ref, f"large scores gain={gain} causal={causal}", vabs=va_ref)
 
 
 def test_dense_outlier_keys_small():
@@ -85,8 +84,8 @@ def test_dense_outlier_keys_small():
                       outlier_frac=0.01, outlier_gain=8.0)
     t = make_dense(w)
     o, lse = run_fa(t["q"], t["k"], t["v"], True, w.scale)
-    o_ref, lse_ref = oracle.get().dense(t["q"], t["k"], t["v"], True, w.scale)
-    compare(o, o_ref, lse, lse_ref, "outliers")
+    o_ref, lse_ref, va_ref = oracle.get().dense(t["q"], t["k"], t["v"], True, w.scale, vabs=True)
+    compare(o, o_ref, lse, lse_ref, "outliers", vabs=va_ref)
 
 
 def test_dense_deterministic():
@@ -120,8 +119,8 @@ def test_dense_reads_and_writes_stay_in_bounds():
     torch.cuda.synchronize()
     assert bool((obuf[:guard] == 3.0).all()) and bool((obuf[guard + n:] == 3.0).all())
     assert bool((lbuf[:guard] == 7.0).all()) and bool((lbuf[guard + B * S * H:] == 7.0).all())
-    o_ref, lse_ref = oracle.get().dense(tensors[0][0], tensors[1][0], tensors[2][0], True, 0.1)
-    compare(bf16_to_f64(out), o_ref, lse.cpu().numpy(), lse_ref, "guarded")
+    o_ref, lse_ref, va_ref = oracle.get().dense(tensors[0][0], tensors[1][0], tensors[2][0], True, 0.1, vabs=True)
+    compare(bf16_to_f64(out), o_ref, lse.cpu().numpy(), lse_ref, "guarded", vabs=va_ref)
 
 
 def _sample_rows(B, S, H, rng, n_random):
@@ -152,11 +151,11 @@ def test_full_size_sampled_rows(name, n_random):
     o, lse = fa.fa_fwd(to_dev(t["q"]), to_dev(t["k"]), to_dev(t["v"]), causal=w.causal, scale=w.scale)
     torch.cuda.synchronize()
     rows = _sample_rows(w.B, w.S, w.Hq, np.random.default_rng(0), n_random)
-    o_ref, lse_ref = oracle.get().dense_rows(t["q"], t["k"], t["v"], w.causal, w.scale, rows)
+    o_ref, lse_ref, va_ref = oracle.get().dense_rows(t["q"], t["k"], t["v"], w.causal, w.scale, rows, vabs=True)
     ridx = torch.from_numpy(rows).cuda()
     o_s = o[ridx[:, 0], ridx[:, 1], ridx[:, 2]]
     l_s = lse[ridx[:, 0], ridx[:, 1], ridx[:, 2]]
-    compare(bf16_to_f64(o_s), o_ref, l_s.cpu().numpy(), lse_ref, name)
+    compare(bf16_to_f64(o_s), o_ref, l_s.cpu().numpy(), lse_ref, name, vabs=va_ref)
     # properties that hold at any size: every row finite, LSE finite
     assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
 
@@ -177,10 +176,10 @@ def test_dense_long_sequence_sampled():
     rng = np.random.default_rng(7)
     idx = np.concatenate([[0, 127, 128, 255, 256, S - 129, S - 128, S - 1], rng.integers(0, S, 24)])
     rows = np.stack([np.zeros_like(idx), idx, rng.integers(0, Hq, len(idx))], axis=1).astype(np.int64)
-    o_ref, lse_ref = oracle.get().dense_rows(q, k, v, True, 1 / math.sqrt(d), rows)
+    o_ref, lse_ref, va_ref = oracle.get().dense_rows(q, k, v, True, 1 / math.sqrt(d), rows, vabs=True)
     ridx = torch.from_numpy(rows).cuda()
     compare(bf16_to_f64(o[ridx[:, 0], ridx[:, 1], ridx[:, 2]]), o_ref,
-            lse[ridx[:, 0], ridx[:, 1], ridx[:, 2]].cpu().numpy(), lse_ref, "dense S=131072")
+            lse[ridx[:, 0], ridx[:, 1], ridx[:, 2]].cpu().numpy(), lse_ref, "dense S=131072", vabs=va_ref)
 
 
 
