@@ -56,7 +56,9 @@ typedef enum {
   FA_ERR_DEVICE_BAD_PAGE = 8  /* a kernel met a page id outside [0, num_pages) (device status) */
 } fa_status;
 
-/* Human-readable name of a status code (static storage, never NULL). */
+/* Human-readable name of a status code (static storage, never NULL). The pages define no error
+ * handling; this boundary reports every failure as a returned code (never an exception or a trap),
+ * and this call names the codes. */
 const char* fa_status_string(fa_status s);
 
 /*
@@ -98,7 +100,11 @@ fa_status fa_paged_fwd(const void* q, const void* k_pages, const void* v_pages,
                        int causal, float scale, void* o, float* lse, void* workspace,
                        size_t workspace_bytes, int num_splits, fa_stream_t stream);
 
-/* Workspace bytes fa_paged_fwd needs for these sizes (same num_splits argument, 0 = auto). */
+/* Workspace bytes fa_paged_fwd needs for these sizes (same num_splits argument, 0 = auto). The
+ * pages name no workspace: it exists because the caller owns all device memory (the library never
+ * allocates), so the caller must learn how much scratch a call needs -- the planned work list and,
+ * when keys are split, the fp32 partial states the LSE merge combines. It takes the same shape
+ * arguments as the call it sizes because the plan (GQA packing, key splits) depends on them. */
 size_t fa_paged_workspace_bytes(int num_seqs, int total_q, int max_q_len, int page_size,
                                 int max_pages_per_seq, int num_pages, int Hq, int Hkv, int d,
                                 int num_splits);
@@ -193,16 +199,19 @@ fa_status fa_paged_append(const void* k_new, const void* v_new, const int32_t* c
  * example an engine whose device memory is all handed to a fixed arena, or a plugin inside a
  * host that owns every allocation) and so cannot lend fa_paged_fwd a workspace.
  *   Arguments and results are those of fa_paged_fwd for a decode batch (every query length is
- *   0 or 1, i.e. max_q_len == 1); inputs and outputs are still the caller's. It always runs the
- *   split-KV CUDA-core decode kernel, which takes GQA groups (Hq / Hkv) of 1, 2, 4 and 8; other
- *   groups return FA_ERR_UNSUPPORTED.
+ *   0 or 1, i.e. max_q_len == 1); inputs and outputs are still the caller's. total_q must be at
+ *   most num_seqs (FA_ERR_INVALID_ARG otherwise) and num_seqs at most 65535 (FA_ERR_UNSUPPORTED
+ *   otherwise), both checked before anything is enqueued. It always runs the split-KV CUDA-core
+ *   decode kernel, which takes GQA groups (Hq / Hkv) of 1, 2, 4 and 8; other groups return
+ *   FA_ERR_UNSUPPORTED.
  *   Scratch: the per-split partials live in a fixed device array of FA_NOALLOC_SCRATCH_BYTES
  *   (16 MiB) inside this library, which every GPU that loads the library holds until the process
  *   exits. The function itself allocates and frees nothing.
- *   num_splits > 0 whose scratch (num_splits * num_seqs * Hq * (d + 1) floats of partials plus
- *   one int per sequence and block of up to 8 kv heads, each part 256-byte aligned) exceeds the
- *   array is rejected with FA_ERR_WORKSPACE before anything is enqueued; num_splits == 0 lowers
- *   the automatic count until it fits.
+ *   A split count is first capped at max_pages_per_seq. num_splits > 0 whose scratch after that
+ *   cap (splits * num_seqs * Hq * (d + 1) floats of partials plus one int per sequence and block
+ *   of up to 8 kv heads, each part 256-byte aligned) exceeds the array is rejected with
+ *   FA_ERR_WORKSPACE before anything is enqueued; num_splits == 0 lowers the automatic count
+ *   (fa_decode_num_splits) until it fits.
  *   Sharing: every call on a device uses the same scratch, which keeps the last call's contents;
  *   the merge counters in it are cleared by each call (an asynchronous memset on `stream`). Calls
  *   whose kernels overlap on the GPU -- on two streams, or from two threads -- race on it; order
@@ -219,7 +228,9 @@ fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages, const void
                                   fa_stream_t stream);
 
 /*
- * Read and clear this GPU's device status word. Synchronises `stream` first.
+ * Read and clear this GPU's device status word. Synchronises `stream` first. The pages define no
+ * failure reporting; kernels here never trap, so a device-side failure (a bounded wait that gave
+ * up, a page id outside the pool) is recorded in this word and read back through this call.
  * *code receives FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BAD_PAGE; *site (may be NULL) a
  * small id of the place in the kernels that recorded it. Returns FA_ERR_CUDA if the synchronisation itself failed.
  */

@@ -120,6 +120,20 @@ def _i32_cuda(name, t):
         raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
 
 
+def _check_outputs(out, lse, o_shape, like, out_dtype=torch.bfloat16):
+    """A caller-given output must have exactly the shape, dtype and device the kernels write: a
+    smaller buffer would be written past its end."""
+    if out is not None:
+        if (not isinstance(out, torch.Tensor) or out.dtype != out_dtype or out.device != like.device
+                or tuple(out.shape) != tuple(o_shape) or not out.is_contiguous()):
+            raise ValueError(f"out must be a contiguous {out_dtype} tensor of shape {tuple(o_shape)} on {like.device}")
+    if lse is not None:
+        l_shape = tuple(o_shape[:-1])
+        if (not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32 or lse.device != like.device
+                or tuple(lse.shape) != l_shape or not lse.is_contiguous()):
+            raise ValueError(f"lse must be a contiguous float32 tensor of shape {l_shape} on {like.device}")
+
+
 def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
     """Dense attention forward. q: [B, S, Hq, d]; k, v: [B, S, Hkv, d] (bf16, CUDA).
 
@@ -132,6 +146,7 @@ def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=Tru
     if k.shape != (B, S, Hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, S, Hkv, d] matching q")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check_outputs(out, lse, q.shape, q)
     with _on(stream):
         if out is None:
             out = torch.empty_like(q)
@@ -178,6 +193,7 @@ def fa_paged_fwd(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, max_q_l
     if dk != d or v_pages.shape != k_pages.shape:
         raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check_outputs(out, lse, q.shape, q)
     need = fa_paged_workspace_bytes(num_seqs, total_q, max_q_len, page_size, max_pages, num_pages, Hq, Hkv, d,
                                     num_splits)
     with _on(stream):
@@ -206,6 +222,7 @@ def fa_merge_states(o_parts, lse_parts, out=None, lse=None, return_lse=True, str
     P, n, H, d = o_parts.shape
     if lse_parts.shape != (P, n, H):
         raise ValueError("lse_parts must be [P, n, H]")
+    _check_outputs(out, lse, (n, H, d), o_parts)
     with _on(stream):
         if out is None:
             out = torch.empty((n, H, d), dtype=torch.bfloat16, device=o_parts.device)
@@ -240,6 +257,7 @@ def fa_cascade_fwd(q, k_pages, v_pages, cu_q_groups, prefix_page_table, prefix_l
         raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]")
     if cu_q_groups.shape != (num_groups + 1,) or prefix_lens.shape != (num_groups,):
         raise ValueError("cu_q_groups must be [num_groups + 1] and prefix_lens [num_groups]")
+    _check_outputs(out, lse, q.shape, q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     lib = load_library()
     need = lib.fa_cascade_workspace_bytes(num_groups, num_seqs, total_q, int(max_group_q_len), int(max_q_len),
@@ -319,8 +337,11 @@ def fa_paged_decode_noalloc(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_le
     for name, t in (("page_table", page_table), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens)):
         _i32_cuda(name, t)
     total_q, Hq, d = q.shape
-    num_pages, page_size, Hkv, _ = k_pages.shape
+    num_pages, page_size, Hkv, dk = k_pages.shape
     num_seqs, max_pages = page_table.shape
+    if dk != d or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]")
+    _check_outputs(out, lse, q.shape, q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     code = load_library().fa_paged_decode_noalloc(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens), num_seqs,

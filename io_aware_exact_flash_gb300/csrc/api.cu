@@ -349,6 +349,7 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   if (max_q_len == 1 && !decode_on_tensor_cores(group)) {
     // ------------------------------------------------------------- split-KV decode
     if (group != 1 && group != 2 && group != 4 && group != 8) return FA_ERR_UNSUPPORTED;
+    if (num_seqs > fa::kDecodeMaxSeqs) return FA_ERR_UNSUPPORTED;
     const DecodePlan dp =
         plan_decode(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv, num_splits, dev->sm_count);
     const size_t need = decode_workspace(num_seqs, Hq, Hkv, d, dp.splits);

@@ -416,6 +416,7 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
       }
     }
   }
+  if (p.num_seqs > kDecodeMaxSeqs || p.Hkv / p.heads_per_cta > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid(p.num_splits, p.num_seqs, p.Hkv / p.heads_per_cta);
   if (p.num_splits > 1) {
     // arrival counters of the fused merge start at zero on every call

@@ -72,6 +72,10 @@ struct DecodeParams {
   DeviceStatus* status;
 };
 
+// The CUDA-core decode kernel's grid has one y index per sequence, so a batch holds at most this
+// many sequences on that kernel.
+constexpr int kDecodeMaxSeqs = 65535;
+
 // kv heads one decode CTA handles: the largest divisor of Hkv that is at most 8
 inline int decode_heads_per_cta(int Hkv) {
   int h = Hkv <= 8 ? Hkv : 8;

@@ -60,6 +60,9 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages,
   if (num_seqs <= 0 || total_q < 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0 || Hq <= 0 ||
       Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0 || !std::isfinite(scale) || !(scale > 0.f))
     return FA_ERR_INVALID_ARG;
+  // decode only: every sequence has at most one query row, so there are at most num_seqs rows
+  if (total_q > num_seqs) return FA_ERR_INVALID_ARG;
+  if (num_seqs > fa::kDecodeMaxSeqs) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FA_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
@@ -72,17 +75,17 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_pages,
       misaligned(kv_lens, 4))
     return FA_ERR_ALIGNMENT;
 
-  // Explicit split counts whose partials do not fit the scratch are rejected; the automatic
-  // count is lowered until they fit (one split needs no scratch at all).
-  int splits = num_splits;
-  if (splits > 0) {
-    if (partials_bytes(splits, num_seqs, Hq, Hkv, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
-  } else {
-    splits = fa_decode_num_splits(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv);
-    while (splits > 1 && partials_bytes(splits, num_seqs, Hq, Hkv, d) > kNoAllocScratchBytes) --splits;
-  }
+  // A split count never exceeds the pages of the longest sequence. An explicit count whose
+  // partials do not fit the scratch (after that cap) is rejected; the automatic count is lowered
+  // until they fit (one split needs no scratch at all).
+  int splits = num_splits > 0 ? num_splits : fa_decode_num_splits(num_seqs, page_size, max_pages_per_seq, num_pages, Hkv);
   if (splits > max_pages_per_seq) splits = max_pages_per_seq;
   if (splits < 1) splits = 1;
+  if (num_splits > 0) {
+    if (partials_bytes(splits, num_seqs, Hq, Hkv, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+  } else {
+    while (splits > 1 && partials_bytes(splits, num_seqs, Hq, Hkv, d) > kNoAllocScratchBytes) --splits;
+  }
 
   fa::DeviceStatus* status = nullptr;
   int sm_count = 0;

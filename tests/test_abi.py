@@ -178,3 +178,35 @@ def test_key_split_plan_is_host_only():
     assert 2 <= prefix <= 16 and 16 * prefix <= 148  # one wave (148 or 152 SMs), each split >= 8 tiles
     # no split when a pass has more units than three waves, whatever the key length
     assert binding.fa_paged_num_splits(64, 64 * 512, 512, 16, 1024, 70000, 32, 8, 128) == 1
+
+
+def _noalloc(lib, **kw):
+    a = dict(q=FAKE, kp=FAKE, vp_=FAKE, pt=FAKE, cu=FAKE, kl=FAKE, num_seqs=4, total_q=4, ps=16, max_pages=64,
+             num_pages=256, Hq=32, Hkv=8, d=128, scale=0.1, o=FAKE, lse=None, splits=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.fa_paged_decode_noalloc(vp(a["q"]), vp(a["kp"]), vp(a["vp_"]), vp(a["pt"]), vp(a["cu"]), vp(a["kl"]),
+                                       a["num_seqs"], a["total_q"], a["ps"], a["max_pages"], a["num_pages"], a["Hq"],
+                                       a["Hkv"], a["d"], a["scale"], vp(a["o"]), vp(a["lse"]) if a["lse"] else None,
+                                       a["splits"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(num_seqs=0), 1), (dict(total_q=5), 1), (dict(Hq=12), 1), (dict(splits=-1), 1),
+    (dict(num_seqs=70000, total_q=70000), 2), (dict(Hq=48, Hkv=3), 2), (dict(d=96), 2), (dict(ps=8), 2),
+    (dict(o=FAKE + 8), 3),
+    # 64 splits x 1024 sequences x 32 heads x 129 floats: far above the 16 MiB scratch
+    (dict(num_seqs=1024, total_q=1024, splits=64), 4),
+])
+def test_fa_paged_decode_noalloc_host_validation(lib, kw, code):
+    """Rows beyond one per sequence, grids the decode kernel cannot launch and split counts whose
+    partials do not fit the fixed scratch are refused on the host, before anything is enqueued."""
+    assert _noalloc(lib, **kw) == code
+
+
+def test_fa_paged_decode_noalloc_caps_splits_before_the_scratch_check(lib):
+    """64 splits of 4-page sequences are capped at 4, which fit (4 x 128 sequences x 32 heads x 129
+    floats): validation passes (the call then needs a device, so on a machine without one it fails
+    later, with another code). Uncapped, the same 64 splits would not fit."""
+    assert _noalloc(lib, num_seqs=128, total_q=128, max_pages=64, splits=64) == 4
+    assert _noalloc(lib, num_seqs=128, total_q=128, max_pages=4, splits=64) not in (1, 2, 3, 4)
