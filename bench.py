@@ -49,12 +49,13 @@ HEADLINE = "causal_prefill_b4_h32_s4096_d128"
 EXTRAS = ["gqa_causal_prefill_b1_hq32_hkv8_s32768_d128", "paged_prefill_64seq_512_8192_hq32_hkv8_d128_p16",
           "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16", "paged_append_64seq_512_8192_hkv8_d128_p16",
           "cascade_decode_128seq_prefix16384_suffix256_2048_hq32_hkv8_d128_p16",
-          "mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16", "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16"]
+          "mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16", "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16",
+          "paged_decode_16seq_1024_16384_hq32_hkv8_d128_p16",
+          "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16@splits=4"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) of one headline prefill launch from the ncu capture summarised in
-# profiles/prefill_kernel_causal_b4_h32_s4096_d128.md, and the kernel state it was taken on (the
-# digest of its sources without comments); the bench reports it as roofline.traffic only while
-# that code is unchanged.
+# DRAM bytes (read + write) of one headline prefill launch from an ncu capture, and the kernel
+# state it was taken on (the digest of its sources without comments); the bench reports it as
+# roofline.traffic only while that code is unchanged.
 PREFILL_TRAFFIC = {"bytes": 429091840 + 113318912,
                    "source_sha256": "917b301208b2704c13aff043a4c119065699d7c7765b594da6a427078f7cbd1c"}
 L2_FLUSH_BYTES = 512 << 20
@@ -217,12 +218,16 @@ class DenseCase:
 
 
 class PagedCase:
-    def __init__(self, name, device):
+    """A paged workload through fa_paged_fwd; num_splits > 0 forces that many key splits (their
+    partial states then go through the LSE merge), 0 lets the planner choose."""
+
+    def __init__(self, name, device, num_splits=0):
         import torch
 
         import io_aware_exact_flash_gb300 as fa
 
         self.w = WORKLOADS[name]
+        self.num_splits = num_splits
         t = make_paged(self.w)
         self.host = t
         self.q = to_dev(t["q"], device)
@@ -232,7 +237,8 @@ class PagedCase:
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
         need = fa.fa_paged_workspace_bytes(self.w.num_seqs, t["total_q"], self.max_q, self.w.page_size,
-                                           t["page_table"].shape[1], t["num_pages"], self.w.Hq, self.w.Hkv, self.w.d)
+                                           t["page_table"].shape[1], t["num_pages"], self.w.Hq, self.w.Hkv, self.w.d,
+                                           num_splits)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.scores = paged_allowed_scores(t, self.w.Hq, self.w.causal)
         self.flops = 4.0 * self.w.d * self.scores
@@ -242,9 +248,11 @@ class PagedCase:
         kv_rows = int(t["kv_lens"].astype(np.int64).sum())
         self.bytes = (2 * kv_rows * self.w.Hkv * self.w.d * 2 + t["total_q"] * self.w.Hq * self.w.d * 2 * 2
                       + t["total_q"] * self.w.Hq * 4)
-        self.splits = fa.fa_paged_num_splits(self.w.num_seqs, t["total_q"], self.max_q, self.w.page_size,
-                                             t["page_table"].shape[1], t["num_pages"], self.w.Hq, self.w.Hkv,
-                                             self.w.d)
+        self.splits = num_splits if num_splits > 0 else fa.fa_paged_num_splits(
+            self.w.num_seqs, t["total_q"], self.max_q, self.w.page_size, t["page_table"].shape[1], t["num_pages"],
+            self.w.Hq, self.w.Hkv, self.w.d)
+        max_tiles = (t["page_table"].shape[1] * self.w.page_size + 127) // 128
+        self.splits = min(self.splits, max_tiles)
         g = self.w.Hq // self.w.Hkv
         # decode runs on the tensor cores unless FA_DECODE_TC=0 sends it to the CUDA-core kernel
         self.tensor_cores = not (self.w.decode and os.environ.get("FA_DECODE_TC") == "0" and g in (1, 2, 4, 8))
@@ -253,7 +261,7 @@ class PagedCase:
         import io_aware_exact_flash_gb300 as fa
 
         fa.fa_paged_fwd(self.q, self.kp, self.vp, self.pt, self.cu, self.kl, self.max_q, causal=self.w.causal,
-                        scale=self.w.scale, out=self.o, lse=self.lse, workspace=self.ws)
+                        scale=self.w.scale, out=self.o, lse=self.lse, workspace=self.ws, num_splits=self.num_splits)
 
     @property
     def launches(self):
@@ -355,6 +363,10 @@ class FlatView:
 
 
 def make_case(name, device):
+    """name is a workload name, optionally followed by "@splits=N" to force N key splits."""
+    if "@splits=" in name:
+        base, n = name.split("@splits=")
+        return PagedCase(base, device, num_splits=int(n))
     w = WORKLOADS[name]
     if isinstance(w, CascadeWorkload):
         return CascadeCase(name, device)
@@ -510,16 +522,19 @@ def profile_only(args, device):
 
     import torch
 
-    w = WORKLOADS[args.only]
+    base = args.only.split("@")[0]
+    w = WORKLOADS[base]
     if args.seqs is not None:
         if not hasattr(w, "num_seqs"):
             raise SystemExit("--seqs applies to paged workloads")
-        WORKLOADS[args.only] = dataclasses.replace(w, num_seqs=args.seqs)
+        WORKLOADS[base] = dataclasses.replace(w, num_seqs=args.seqs)
     case = make_case(args.only, device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     ms = statistics.mean(time_case(case, args.steps, args.warmup, flush))
     if case.kind in ("decode", "append", "cascade", "verify"):
         out = {"workload": args.only, "seqs": case.w.num_seqs, "ms": ms, "GB/s": case.bytes / (ms * 1e-3) / 1e9}
+        if isinstance(case, PagedCase):
+            out["splits"] = case.splits
         if case.kind == "cascade":
             out["flat_paged_fwd_ms"] = statistics.mean(time_case(FlatView(case), args.steps, args.warmup, flush))
     else:

@@ -294,6 +294,11 @@ WORKLOADS = {
     "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16": PagedWorkload(
         "paged_decode_128seq_1024_16384_hq32_hkv8_d128_p16", num_seqs=128, len_lo=1024,
         len_hi=16384, Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=True, seed=1004),
+    # a small decode batch of the same length distribution: too few (sequence, kv head) units to
+    # fill the GPU, so the keys are split and the partial states merged by their LSE
+    "paged_decode_16seq_1024_16384_hq32_hkv8_d128_p16": PagedWorkload(
+        "paged_decode_16seq_1024_16384_hq32_hkv8_d128_p16", num_seqs=16, len_lo=1024,
+        len_hi=16384, Hq=32, Hkv=8, d=128, page_size=16, causal=True, decode=True, seed=1008),
     # one launch mixing full prefill (16 seqs), chunked prefill (16 seqs, chunks of 1..512 new
     # tokens behind their cached keys) and decode (32 seqs), kv_len 512..8192
     "mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16": PagedWorkload(
