@@ -227,13 +227,17 @@ __device__ __forceinline__ int unit_of_round(int r) {
 
 // Work items of the dense launches: one unit, or under causal masking a mirrored pair of units —
 // query-tile pair i and its mirror T-1-i of one query head, heaviest first. Every pair then costs
-// the same, so CTAs stay balanced. Returns unit `sub` of item `item` as an index of the dense
-// order (unit_at), or -1 when the item has no such unit.
+// the same, so CTAs stay balanced. Sets u0 and u1 to the item's units as indices of the dense order
+// (unit_at); -1 where the item has no such unit.
 template <bool PAGED>
-__device__ __forceinline__ int item_unit(const PrefillParams& p, int item, int sub, int n_units) {
-  if (!p.pair_units) return sub == 0 && item < n_units ? item : -1;
+__device__ __forceinline__ void item_units(const PrefillParams& p, int item, int n_units, int& u0, int& u1) {
+  u1 = -1;
+  if (!p.pair_units) {
+    u0 = item < n_units ? item : -1;
+    return;
+  }
   if constexpr (PAGED) {
-    return -1;
+    u0 = -1;
   } else {
     const int T = (p.S + 2 * kBM - 1) / (2 * kBM);
     const int half = (T + 1) / 2;  // pairs per query head
@@ -246,9 +250,8 @@ __device__ __forceinline__ int item_unit(const PrefillParams& p, int item, int s
     const int rc = item - chunk * pairs_per_chunk;
     const int i = rc / width, head = rc % width;
     const int chunk_start = chunk * p.kv_heads_per_chunk * G * T;
-    if (sub == 0) return chunk_start + i * width + head;                              // qt2 = T-1-i
-    if (sub == 1 && T - 1 - i != i) return chunk_start + (T - 1 - i) * width + head;  // qt2 = i
-    return -1;
+    u0 = chunk_start + i * width + head;                                       // qt2 = T-1-i
+    if (T - 1 - i != i) u1 = chunk_start + (T - 1 - i) * width + head;          // qt2 = i
   }
 }
 
@@ -267,36 +270,41 @@ constexpr int kUnitWalkers = 11;  // warps 0-2 and 4-11
 // L2-aware unit order) while a CTA's set-up — barriers, TMEM, the first loads — is paid once per
 // SM rather than once per item, and the next item's first loads overlap this item's tail.
 struct Cursor {
-  int item, sub;   // current item and its next unit
+  int u0, u1;      // the current item's units (-1: none)
+  int sub;         // units of the current item handed out so far
   uint32_t taken;  // responses read so far
+  // true once the current item has no unit left to hand out
+  __device__ __forceinline__ bool item_done() const { return sub >= 2 || (sub == 1 && u1 < 0); }
 };
+
+template <bool PAGED>
+__device__ __forceinline__ Cursor first_cursor(const PrefillParams& p, int n_units) {
+  Cursor c{-1, -1, 0, 0u};
+  item_units<PAGED>(p, (int)blockIdx.x, n_units, c.u0, c.u1);
+  return c;
+}
 
 template <bool PAGED, bool TAKE>
 __device__ __forceinline__ int next_unit(const PrefillParams& p, Cursor& c, int r, int n_units, TakeOver& t,
                                          volatile int* abort) {
   if constexpr (!TAKE) {
-    if (p.pair_units) return r < 2 ? item_unit<PAGED>(p, blockIdx.x, r, n_units) : -1;
+    if (p.pair_units) return r == 0 ? c.u0 : (r == 1 ? c.u1 : -1);
     const int u = unit_of_round(r);
     return u < n_units ? u : -1;
   } else {
-    for (;;) {
-      if (c.sub < 2) {
-        const int u = item_unit<PAGED>(p, c.item, c.sub++, n_units);
-        if (u >= 0) return u;
-        continue;
-      }
-      const uint32_t s = c.taken & 1, parity = (c.taken >> 1) & 1;
-      ++c.taken;
-      int item = -1;
-      if (mbar_wait(&t.full[s], parity, abort, p.status, kSiteTakeOver)) item = launch_cancel_result(&t.resp[s]);
-      item = __shfl_sync(0xffffffffu, item, 0);  // lane 0 decides for its warp
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&t.empty[s]);
-      // A failed request, or an item without units (a grid that is an upper bound ends with such
-      // items), ends the walk: the producer asks for another item only after loading a unit.
-      if (item < 0 || item_unit<PAGED>(p, item, 0, n_units) < 0) return -1;
-      c.item = item;
-      c.sub = 0;
-    }
+    if (!c.item_done()) return c.sub++ == 0 ? c.u0 : c.u1;
+    const uint32_t s = c.taken & 1, parity = (c.taken >> 1) & 1;
+    ++c.taken;
+    int item = -1;
+    if (mbar_wait(&t.full[s], parity, abort, p.status, kSiteTakeOver)) item = launch_cancel_result(&t.resp[s]);
+    item = __shfl_sync(0xffffffffu, item, 0);  // lane 0 decides for its warp
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&t.empty[s]);
+    // A failed request, or an item without units (a grid that is an upper bound ends with such
+    // items), ends the walk: the producer asks for another item only after loading a unit.
+    c.u0 = -1;
+    if (item >= 0) item_units<PAGED>(p, item, n_units, c.u0, c.u1);
+    c.sub = 1;
+    return c.u0;
   }
 }
 
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const uint64_t kv_policy = policy_evict_last();
     const uint64_t q_policy = policy_evict_first();
     uint32_t kv_it = 0;  // position in the K/V ring, continued across units
-    Cursor cur{(int)blockIdx.x, 0, 0u};
+    Cursor cur = first_cursor<PAGED>(p, n_units);
     uint32_t requests = 0;  // launch cancellations requested
     for (int r = 0;; ++r) {
       const int u = next_unit<PAGED, TAKE>(p, cur, r, n_units, take, abort);
@@ -439,7 +447,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       // The item's last unit is loaded: ask for the next item now, about a ring's depth of key
       // tiles before the walkers need it. One request is in flight at a time, and none follows a
       // failed one (the walk ends there).
-      if (TAKE && item_unit<PAGED>(p, cur.item, cur.sub, n_units) < 0) {
+      if (TAKE && cur.item_done()) {
         int issued = 0;
         if (lane == 0 && !*abort) {
           const uint32_t s = requests & 1;  // the slot's previous response must have been read
@@ -496,7 +504,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       mbar_arrive(&bar_turn[1 - g]);
       ++turn;
     };
-    Cursor cur{(int)blockIdx.x, 0, 0u};
+    Cursor cur = first_cursor<PAGED>(p, n_units);
     for (int r = 0;; ++r) {
       const int u = next_unit<PAGED, TAKE>(p, cur, r, n_units, take, abort);
       if (u < 0) break;
@@ -613,7 +621,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const uint32_t tO = tmem + C::kColO + g * D + lane_off;
     const float sl2 = p.scale_log2;
     uint32_t tcnt = 0, ounits = 0;
-    Cursor cur{(int)blockIdx.x, 0, 0u};
+    Cursor cur = first_cursor<PAGED>(p, n_units);
     for (int r = 0;; ++r) {
       const int u = next_unit<PAGED, TAKE>(p, cur, r, n_units, take, abort);
       if (u < 0) break;
@@ -639,6 +647,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           continue;
         }
         tc_fence_after();
+        const int valid = lim_row - (w.kv_t0 + j) * kBN;
+        if (__any_sync(0xffffffffu, valid < kBN)) {
+          // Tiles that cross the diagonal or the end of the keys: the masked scores are set to
+          // -inf in TMEM, one 32-column chunk at a time in a loop that is not unrolled, so that
+          // this rarely taken path adds little code to the loop every tile runs.
+#pragma unroll 1
+          for (int cc = 0; cc < kBN / 32; ++cc) {
+            uint32_t mr[32];
+            tmem_ld32(tS + cc * 32, mr);
+            tmem_ld_wait(mr);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (cc * 32 + c >= valid) mr[c] = 0xff800000u;  // -inf
+            tmem_st32(tS + cc * 32, mr);
+          }
+          tmem_st_wait();
+        }
         uint32_t sr[kBN];
         tmem_ld32(tS + 0, sr + 0);
         tmem_ld32(tS + 32, sr + 32);
@@ -648,12 +673,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         tmem_ld_wait(sr + 32);
         tmem_ld_wait(sr + 64);
         tmem_ld_wait(sr + 96);
-        const int valid = lim_row - (w.kv_t0 + j) * kBN;
-        if (valid < kBN) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= valid) sr[c] = 0xff800000u;  // -inf
-        }
         const float m_tile = row_max_chunks<0, 4>(sr) * sl2;
         const bool need = m_tile > m_run + kRescaleThreshold;
         const float alpha = need ? ex2(m_run - m_tile) : 1.f;  // 0 while m_run is -inf
@@ -664,13 +683,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         // O rescale (after P is written, so S no longer occupies registers): P V of the previous
         // tile is complete, because the commit that signalled this tile's S was issued after it.
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
+          // rare: a loop that is not unrolled keeps the code small
+          const uint64_t a2 = f32x2(alpha, alpha);
+#pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t orr[32];
             tmem_ld32(tO + cc * 32, orr);
             tmem_ld_wait(orr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * alpha);
+            for (int i = 0; i < 16; ++i) {
+              float a, b;
+              split_f32x2(mul_f32x2(f32x2(u2f(orr[2 * i]), u2f(orr[2 * i + 1])), a2), a, b);
+              orr[2 * i] = f2u(a);
+              orr[2 * i + 1] = f2u(b);
+            }
             tmem_st32(tO + cc * 32, orr);
           }
         }
@@ -680,26 +706,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         __syncwarp();
       }
       // ------------------------------------------------------------ epilogue: O / l, LSE
-      uint32_t orr[D];
-      if (nkv > 0) {
-        mbar_wait(&bar_o[g], ounits & 1, abort, p.status, kSiteSoftmaxO);
-        __syncwarp();
-        ++ounits;
-        if (!live) {
-          mbar_arrive(&bar_o_free[g]);
-          continue;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, orr + cc * 32);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(orr + cc * 32);
-        tc_fence_before();
-        mbar_arrive(&bar_o_free[g]);  // the MMA may now overwrite O with the next unit
-      } else {
-#pragma unroll
-        for (int i = 0; i < D; ++i) orr[i] = 0u;
-      }
+      // O is read from TMEM and stored one 32-column chunk at a time, in a loop that is not
+      // unrolled (this code runs once per unit; small code keeps the per-tile loop in the
+      // instruction cache). The MMA may overwrite O once every chunk has been read.
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const int64_t tok = w.tok0 + row;
       const bool store = row < w.q_len && (!PAGED || tok < p.total_q);
@@ -712,20 +721,46 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         lse_out = p.lse_part;
         orow += (int64_t)w.split * p.total_q * p.Hq;
       }
-      if (store && o_f32 != nullptr) {
-        float4* dst = reinterpret_cast<float4*>(o_f32 + orow * D);
+      if (nkv > 0) {
+        mbar_wait(&bar_o[g], ounits & 1, abort, p.status, kSiteSoftmaxO);
+        __syncwarp();
+        ++ounits;
+        if (!live) {
+          mbar_arrive(&bar_o_free[g]);
+          continue;
+        }
+        tc_fence_after();
+      }
+      const uint64_t il2 = f32x2(inv_l, inv_l);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t orr[32];
+        if (nkv > 0) {
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+        } else {
 #pragma unroll
-        for (int i = 0; i < D / 4; ++i)
-          dst[i] = make_float4(u2f(orr[4 * i + 0]) * inv_l, u2f(orr[4 * i + 1]) * inv_l,
-                               u2f(orr[4 * i + 2]) * inv_l, u2f(orr[4 * i + 3]) * inv_l);
-      } else if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow * D);
+          for (int i = 0; i < 32; ++i) orr[i] = 0u;
+        }
+        float on[32];
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-          dst[i] = make_uint4(pack_bf16x2(u2f(orr[8 * i + 0]) * inv_l, u2f(orr[8 * i + 1]) * inv_l),
-                              pack_bf16x2(u2f(orr[8 * i + 2]) * inv_l, u2f(orr[8 * i + 3]) * inv_l),
-                              pack_bf16x2(u2f(orr[8 * i + 4]) * inv_l, u2f(orr[8 * i + 5]) * inv_l),
-                              pack_bf16x2(u2f(orr[8 * i + 6]) * inv_l, u2f(orr[8 * i + 7]) * inv_l));
+        for (int i = 0; i < 16; ++i)
+          split_f32x2(mul_f32x2(f32x2(u2f(orr[2 * i]), u2f(orr[2 * i + 1])), il2), on[2 * i], on[2 * i + 1]);
+        if (store && o_f32 != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(o_f32 + orow * D + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[i] = make_float4(on[4 * i], on[4 * i + 1], on[4 * i + 2], on[4 * i + 3]);
+        } else if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow * D + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16x2(on[8 * i + 0], on[8 * i + 1]), pack_bf16x2(on[8 * i + 2], on[8 * i + 3]),
+                                pack_bf16x2(on[8 * i + 4], on[8 * i + 5]), pack_bf16x2(on[8 * i + 6], on[8 * i + 7]));
+        }
+      }
+      if (nkv > 0) {
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[g]);  // the MMA may now overwrite O with the next unit
       }
       if (store && lse_out != nullptr) lse_out[orow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
       __syncwarp();

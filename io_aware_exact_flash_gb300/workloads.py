@@ -285,6 +285,9 @@ WORKLOADS = {
         "dense_noncausal_b1_h2_s256_d64", B=1, S=256, Hq=2, Hkv=2, d=64, causal=False, seed=1000),
     "causal_prefill_b4_h32_s4096_d128": DenseWorkload(
         "causal_prefill_b4_h32_s4096_d128", B=4, S=4096, Hq=32, Hkv=32, d=128, causal=True, seed=1001),
+    # the headline shape at the small workload's head dim (64)
+    "causal_prefill_b4_h32_s4096_d64": DenseWorkload(
+        "causal_prefill_b4_h32_s4096_d64", B=4, S=4096, Hq=32, Hkv=32, d=64, causal=True, seed=1009),
     "gqa_causal_prefill_b1_hq32_hkv8_s32768_d128": DenseWorkload(
         "gqa_causal_prefill_b1_hq32_hkv8_s32768_d128", B=1, S=32768, Hq=32, Hkv=8, d=128, causal=True,
         seed=1002, act_scale=0.5, outlier_frac=0.01, outlier_gain=8.0),
