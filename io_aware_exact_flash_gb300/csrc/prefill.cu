@@ -490,8 +490,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     // The issuers take turns (0, 1, 0, 1, ...) and issue a step's MMAs only on their turn. That
     // keeps the tensor core's work in the order P0 V, Q0 K^T, P1 V, Q1 K^T, ...: one tile's
     // softmax runs while the tensor core serves the other tile. Without turns the two tiles drift
-    // into lockstep, both softmaxes run at once and the tensor core idles meanwhile. Each issuer
-    // takes the same number of turns per unit (one for the first Q K^T, one per key tile).
+    // into lockstep, both softmaxes run at once and the tensor core idles meanwhile. Turns are
+    // taken only at the steps where both tiles issue MMAs (the first Q K^T, then every key tile
+    // both tiles attend to): both issuers know both tiles' key-tile counts, so they skip the same
+    // steps. A unit with one query tile (decode, verify) then takes no turns at all.
     uint32_t turn = 0;
     auto take_turn = [&]() {
       if (g == 0) {
@@ -511,6 +513,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       Unit w;
       unit_at<PAGED>(p, u, w);
       const int nkv = g == 0 ? w.nkv[0] : w.nkv[1];
+      const int nkv_both = min(w.nkv[0], w.nkv[1]);  // key tiles at which both tiles issue MMAs
       if (lane == 0) {
         mbar_wait(&bar_q_full, r & 1, abort, p.status, kSiteMmaQ);
         if (nkv <= 0) mma_commit(&bar_q_empty);  // this tile reads no Q this unit
@@ -522,12 +525,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           // also when its tile does not read the stage: an issuer can then never arrive twice on
           // one pending phase, because the next fill waits for that phase to complete.
           mbar_wait(&bar_full[ks0], (kv_it / NS) & 1, abort, p.status, kSiteMmaFull);
-          take_turn();
+          if (nkv_both > 0) take_turn();
           if (nkv > 0) {
             tc_fence_after();
             issue_qk<D>(tS, dq, dk + ks0 * (TB >> 4), idesc_s);
           }
-          pass_turn();
+          if (nkv_both > 0) pass_turn();
           if (nkv > 0) {
             mma_commit(&bar_s[g]);
             if (nkv == 1) mma_commit(&bar_q_empty);  // the unit's last Q K^T of this tile
@@ -540,7 +543,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           const bool has_next = j + 1 < w.nmax;
           if (lane == 0) mbar_wait(&bar_full[vs], (vi / NS) & 1, abort, p.status, kSiteMmaFull);
           __syncwarp();
-          bool turn_open = false;
           if (j < nkv) {
             if constexpr (PAGED) {
               // Rows of the sequence's partial last page past kv_len hold no valid value (possibly
@@ -567,12 +569,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
               // the first P V of a unit overwrites O: the previous unit's O must have been read
               if (j == 0 && ounits > 0) mbar_wait(&bar_o_free[g], (ounits - 1) & 1, abort, p.status, kSiteMmaP);
               if (j + 1 < nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
-              take_turn();
-              turn_open = true;
+              if (j < nkv_both) take_turn();
               tc_fence_after();
               issue_pv<D>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
               if (j + 1 < nkv) issue_qk<D>(tS, dq, dk + ks * (TB >> 4), idesc_s);
-              pass_turn();
+              if (j < nkv_both) pass_turn();
               if (j == nkv - 1) {
                 mma_commit(&bar_o[g]);
                 ++ounits;
@@ -585,10 +586,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
             ++tcnt;
           }
           if (lane == 0) {
-            if (!turn_open) {  // no MMA of this tile this step: still hand the turn on
-              take_turn();
-              pass_turn();
-            }
             mma_commit(&bar_empty[vs]);
             if (has_next) {
               if (j + 1 >= nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
