@@ -245,6 +245,26 @@ bool decode_on_tensor_cores(int group) {
   return true;
 }
 
+// Batches whose sequences have at most 16 query rows per kv head (decode up to group 16, verify of
+// a few tokens) at d = 128 run on the key-row kernel (decode_tc.cu): the keys of a tile are the
+// MMA's 128 rows and the query rows its columns. Measured against the packed prefill kernel on the
+// decode workload (128 sequences, group 4): 0.744 against 0.763 ms; 16 sequences with 4 key
+// splits 0.098 against 0.112 ms; the cascade's suffix pass takes the cascade from 0.197 to 0.181
+// ms. With 17 to 32 rows (verify of 5-8 tokens at group 4) it measured slower (0.90 against 0.81
+// ms on 128 sequences of 2-8 tokens), so those stay on the packed kernel. FA_DECODE_KEY_ROWS=0
+// sends every batch to the packed kernel, FA_DECODE_KEY_ROWS=2 also the batches of 17-32 rows here.
+int key_row_max_rows() {
+  static std::atomic<int> cache{-1};
+  int v = cache.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char* e = getenv("FA_DECODE_KEY_ROWS");
+    const bool one_char = e != nullptr && e[0] != '\0' && e[1] == '\0';
+    v = (one_char && e[0] == '0') ? 0 : ((one_char && e[0] == '2') ? 32 : 16);
+    cache.store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 // Key splits of the paged tensor-core path. Each (tile pair, head slot) unit becomes kv_splits
 // units over contiguous key ranges, written as fp32 partial states and merged by their LSE
 // afterwards. Splitting pays when there are too few units to fill the GPU a few times over
@@ -398,14 +418,19 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   const size_t need = list_bytes + (external ? 0 : split_parts_bytes(kv_splits, total_q, Hq, d, &lse_off));
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+  // batches of a few query rows per (sequence, kv head) run with the keys on the MMA's rows
+  const int kr_columns = fa::decode_tc_columns(max_q_len, group, d, key_row_max_rows());
   fa::PrefillParams p;
   std::memset(&p, 0, sizeof(p));
   {
     // a Q tile is `pack` heads x (128 / pack) tokens: with pack > 1, row r of the tile is token
-    // r / pack and head r % pack of the box (the box's inner dimensions are d, then heads)
+    // r / pack and head r % pack of the box (the box's inner dimensions are d, then heads). On
+    // the key-row path a unit's Q rows are the group's heads x (columns / group) tokens.
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
     const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
-    const uint32_t box[4] = {64, (uint32_t)pack, (uint32_t)(fa::kBM / pack), 1};
+    const uint32_t box[4] = {64, (uint32_t)(kr_columns > 0 ? group : pack),
+                             (uint32_t)(kr_columns > 0 ? (kr_columns < 16 ? 16 : kr_columns) / group : fa::kBM / pack),
+                             1};
     if (!make_map(&p.tm_q, q, dims, str, box)) return FA_ERR_CUDA;
   }
   {
@@ -447,9 +472,16 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
   }
   p.status = dev->status;
   const int cost_buckets = max_kv_tiles > 8192 ? 8192 : max_kv_tiles;  // buckets only order the work
-  if (fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q, pack), cost_buckets,
-                               work_list, work_count, stream) != cudaSuccess)
+  if (kr_columns > 0) {
+    // one planning item per sequence (at most 32 query rows); the unit's heads are the group
+    p.pack = 1;
+    if (fa::launch_decode_tc(p, kr_columns, dev->sm_count, prefill_max_items(num_seqs, total_q, pack), cost_buckets,
+                             work_list, work_count, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+  } else if (fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q, pack), cost_buckets,
+                                      work_list, work_count, stream) != cudaSuccess) {
     return FA_ERR_CUDA;
+  }
   if (kv_splits > 1 && !external &&
       fa::launch_merge(p.o_part, p.lse_part, kv_splits, total_q, Hq, d, o, o_f32, lse, false, stream) != cudaSuccess)
     return FA_ERR_CUDA;

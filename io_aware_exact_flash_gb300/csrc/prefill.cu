@@ -892,7 +892,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_paged_kernel(
   int run = block_exclusive_scan(mine, warp_sums, &all_items);
   if (tid == 0) {
     total = min(all_items, max_items);  // more items than the host bound means inconsistent lengths
-    *work_count = total;
+    work_count[0] = total;
+    work_count[1] = 0;  // the unit counter of the decode kernel's persistent CTAs
   }
   __syncthreads();
   for (int i = 0; i < per && k0 + i < num_seqs; ++i) {
@@ -981,15 +982,20 @@ cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cu
   return take ? launch_prefill_impl<64, false, true>(q, grid, stream) : launch_prefill_impl<64, false>(q, grid, stream);
 }
 
-cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
-                                 int2* work_list, int* work_count, cudaStream_t stream) {
+cudaError_t launch_plan_paged(const PrefillParams& p, int max_items, int max_kv_tiles, int2* work_list,
+                              int* work_count, cudaStream_t stream) {
   // buckets (at most 8193 ints), or for batches of at most one sequence per thread their counts
   // and order (2 x 1024 ints): within the default dynamic shared memory limit either way
   const int smem = (p.num_seqs <= kPlanThreads ? 2 * kPlanThreads : max_kv_tiles + 1) * (int)sizeof(int);
   int* scratch = reinterpret_cast<int*>(work_list + max_items);  // 2 * num_seqs ints
   plan_paged_kernel<<<1, kPlanThreads, smem, stream>>>(p.cu_seqlens_q, p.kv_lens, p.num_seqs, p.causal, p.pack,
                                                        max_kv_tiles, max_items, work_list, work_count, scratch);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
+                                 int2* work_list, int* work_count, cudaStream_t stream) {
+  cudaError_t e = launch_plan_paged(p, max_items, max_kv_tiles, work_list, work_count, stream);
   if (e != cudaSuccess) return e;
   const long long units = (long long)max_items * (p.Hq / p.pack) * p.kv_splits;
   const int mode = persistent_override();

@@ -242,6 +242,11 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_m
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with A MN-major too (bit 15): A is then read with its M dimension contiguous.
+__host__ __device__ constexpr uint32_t make_idesc_bf16_amn(int M, int N) {
+  return make_idesc_bf16(M, N, false) | (1u << 15);
+}
+
 // Shared-memory matrix descriptor with 128-byte swizzle.
 //   bits 0-13 start>>4, 16-29 leading-dimension byte offset>>4, 32-45 stride-dimension byte
 //   offset>>4, bits 46-48 = 0b001, 61-63 swizzle mode (2 = 128B).
@@ -281,6 +286,38 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t* r) {
                :
                : "memory");
 }
+// 16 consecutive columns per thread; tmem_ld_wait16 ties the 16 registers to the wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+// One column per thread, loaded and waited for.
+__device__ __forceinline__ uint32_t tmem_ld1_sync(uint32_t taddr) {
+  uint32_t v;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v)
+      : "r"(taddr)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v));
+}
+
 // Registers -> TMEM, 32 lanes x 32 bits, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -342,6 +379,12 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+// Maximum of v over the warp's 32 lanes (every lane gets it); NaN inputs are ignored.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 // max of three fp32 values
 __device__ __forceinline__ float max3f(float a, float b, float c) {
