@@ -29,10 +29,13 @@
 // their LSE (merge_kernel).
 //
 // CTA organisation (256 threads):
-//   warp 0      TMA producer: per unit its Q rows, then K_0, V_0, K_1, V_1, ... into a stage ring
+//   warps 0, 2  TMA producers: per unit its Q rows (warp 0), then K_0, V_0, K_1, V_1, ... into a
+//               stage ring, the K tiles from warp 0 and the V tiles from warp 2 (with 16-row pages a
+//               tile is 16 tensor boxes of 2 KB, and one warp's lanes cannot issue them fast enough
+//               to keep up with HBM)
 //   warp 1      MMA issuer (one lane): P V of key tile j and S^T of tile j + 1, S^T first when its
 //               keys have arrived (S^T is double buffered: it then overlaps tile j's softmax)
-//   warp 2      TMEM owner
+//   warp 2      also TMEM owner
 //   warp 3      unit scheduler
 //   warps 4-7   softmax: thread i owns key row i of each tile (TMEM lane i) and, in the epilogue,
 //               row d = i of O^T
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
     for (int b = 0; b < 2 * WG; ++b) mbar_init(&bar_x[b], 4);
     for (int s = 0; s < kUnitSlots; ++s) {
       mbar_init(&bar_u_full[s], 1);
-      mbar_init(&bar_u_empty[s], 2 + 4 * WG);  // producer, issuer and the softmax warps
+      mbar_init(&bar_u_empty[s], 3 + 4 * WG);  // producers, issuer and the softmax warps
     }
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_req, 1);
@@ -286,8 +289,10 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_u_full[slot]);
     }
-  } else if (warp == 0) {
-    // ================================================================ TMA producer
+  } else if (warp == 0 || warp == 2) {
+    // ================================================================ TMA producers
+    // Both walk every unit and the whole ring; warp 0 loads Q and the K stages, warp 2 the V stages.
+    const bool v_warp = warp == 2;
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       int pages_cur = 0, pages_next = 0;
       if (!take_unit(r, x, &pages_cur)) break;
       const int qb = r & 1;
-      if (lane == 0) {
+      if (lane == 0 && !v_warp) {
         if (r >= 2) mbar_wait(&bar_q_empty[qb], ((r >> 1) - 1) & 1, abort, p.status, kSiteKrQ);
         mbar_arrive_expect_tx(&bar_q_full[qb], 2 * q_rows * 128);
 #pragma unroll
@@ -323,12 +328,12 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       // ask for the next unit when the K tile before this unit's last one is loaded (at once for a
       // unit of at most two key tiles): its fetch then overlaps the ring's last tiles of this one
       const int req_idx = x.ntiles >= 2 ? 2 * (x.ntiles - 2) : 0;
-      if (lane == 0 && x.ntiles == 0) mbar_arrive(&bar_req);
+      if (lane == 0 && x.ntiles == 0 && !v_warp) mbar_arrive(&bar_req);
       for (int idx = 0; idx < 2 * x.ntiles; ++idx, ++kv_it) {
         const int j = idx >> 1;
         const bool is_v = idx & 1;
         const int stage = kv_it % NS;
-        if (lane == 0 && idx == req_idx) mbar_arrive(&bar_req);
+        if (lane == 0 && idx == req_idx && !v_warp) mbar_arrive(&bar_req);
         if (!is_v) {
           const int pj = j * ppt;  // the tile's first page within the unit
           if (j > 0 && (pj & 31) == 0) {
@@ -337,6 +342,7 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
           }
           phys = __shfl_sync(0xffffffffu, pages_cur, (pj & 31) + (lane < ppt ? lane : 0));
         }
+        if (is_v != v_warp) continue;  // the other producer's stage
         if (lane == 0) mbar_wait(&bar_empty[stage], ((kv_it / NS) & 1) ^ 1, abort, p.status, kSiteKrEmpty);
         __syncwarp();
         if (lane == 0) mbar_arrive_expect_tx(&bar_full[stage], kStageBytes);
