@@ -248,21 +248,15 @@ bool decode_on_tensor_cores(int group) {
 // Batches whose sequences have at most 16 query rows per kv head (decode up to group 16, verify of
 // a few tokens) at d = 128 run on the key-row kernel (decode_tc.cu): the keys of a tile are the
 // MMA's 128 rows and the query rows its columns. Measured against the packed prefill kernel on the
-// decode workload (128 sequences, group 4): 0.744 against 0.763 ms; 16 sequences with 4 key
-// splits 0.098 against 0.112 ms; the cascade's suffix pass takes the cascade from 0.197 to 0.181
-// ms. With 17 to 32 rows (verify of 5-8 tokens at group 4) it measured slower (0.90 against 0.81
-// ms on 128 sequences of 2-8 tokens), so those stay on the packed kernel. FA_DECODE_KEY_ROWS=0
-// sends every batch to the packed kernel, FA_DECODE_KEY_ROWS=2 also the batches of 17-32 rows here.
+// decode workload (128 sequences, group 4): 0.660 against 0.763 ms; 16 sequences with 4 key
+// splits 0.094 against 0.112 ms; the cascade (its suffix pass) 0.169 against 0.198 ms. Batches
+// of more rows per kv head (verify of 5-8 tokens at group 4) stay on the packed kernel: a 32-column
+// form of the key-row kernel measured 0.77 against 0.81 ms there, but needs a second softmax
+// warpgroup, and 13 warps leave 128 registers a thread (it spilled). FA_DECODE_KEY_ROWS=0 sends
+// every batch to the packed kernel.
 int key_row_max_rows() {
-  static std::atomic<int> cache{-1};
-  int v = cache.load(std::memory_order_relaxed);
-  if (v < 0) {
-    const char* e = getenv("FA_DECODE_KEY_ROWS");
-    const bool one_char = e != nullptr && e[0] != '\0' && e[1] == '\0';
-    v = (one_char && e[0] == '0') ? 0 : ((one_char && e[0] == '2') ? 32 : 16);
-    cache.store(v, std::memory_order_relaxed);
-  }
-  return v;
+  static std::atomic<int> mode{-2};
+  return env_switch("FA_DECODE_KEY_ROWS", &mode) == 0 ? 0 : 16;
 }
 
 // Key splits of the paged tensor-core path. Each (tile pair, head slot) unit becomes kv_splits
@@ -429,8 +423,7 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
     const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
     const uint32_t box[4] = {64, (uint32_t)(kr_columns > 0 ? group : pack),
-                             (uint32_t)(kr_columns > 0 ? (kr_columns < 16 ? 16 : kr_columns) / group : fa::kBM / pack),
-                             1};
+                             (uint32_t)(kr_columns > 0 ? 16 / group : fa::kBM / pack), 1};
     if (!make_map(&p.tm_q, q, dims, str, box)) return FA_ERR_CUDA;
   }
   {

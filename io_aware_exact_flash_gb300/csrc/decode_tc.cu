@@ -8,7 +8,7 @@
 // on chip. Put on the tensor cores the usual way (query rows as the MMA's M = 128 rows), a tile
 // holds only a handful of real rows and each key tile costs a full 128-row Q K^T, softmax and P V
 // chain in series. Here the roles are swapped: a key tile of 128 keys is the MMA's M dimension
-// and the query rows are its N (16 or 32 columns):
+// and the query rows are its N = 16 columns:
 //   S^T[128 keys, N] = K_tile [128, d] . Q^T           (tcgen05.mma, A = K, B = Q, both K-major)
 //   O^T[d, N]       += V_tile^T [d, 128 keys] . P^T    (A = V read MN-major, B = P^T K-major)
 // so each MMA is small, one softmax thread owns one key (one TMEM lane), and the chain per key tile
@@ -28,17 +28,20 @@
 // holds a unit it has not started while others run out of work. Split units write fp32 partial states merged afterwards by
 // their LSE (merge_kernel).
 //
-// CTA organisation (256 threads):
+// CTA organisation (288 threads):
 //   warps 0, 2  TMA producers: per unit its Q rows (warp 0), then K_0, V_0, K_1, V_1, ... into a
 //               stage ring, the K tiles from warp 0 and the V tiles from warp 2 (with 16-row pages a
 //               tile is 16 tensor boxes of 2 KB, and one warp's lanes cannot issue them fast enough
 //               to keep up with HBM)
-//   warp 1      MMA issuer (one lane): P V of key tile j and S^T of tile j + 1, S^T first when its
-//               keys have arrived (S^T is double buffered: it then overlaps tile j's softmax)
+//   warp 1      S^T issuer (one lane): S^T of key tile j as soon as its keys are in and its buffer
+//               is free (S^T is double buffered, so it runs during the previous tile's softmax)
+//   warp 4      P V issuer (one lane): O^T += V^T P^T once the tile's P^T is written. Each
+//               tcgen05.mma issue takes ~100 cycles however small the MMA, so the two streams of
+//               eight MMAs per tile are issued by two warps side by side.
 //   warp 2      also TMEM owner
 //   warp 3      unit scheduler
-//   warps 4-7   softmax: thread i owns key row i of each tile (TMEM lane i) and, in the epilogue,
-//               row d = i of O^T
+//   warps 5-8   softmax: thread i owns key row i of each tile (TMEM lane i, its warp's lane
+//               quarter) and, in the epilogue, row d = i of O^T
 // TMEM columns: S^T buffers at [0, N) and [N, 2N), O^T buffers (one per unit parity) at [2N, 3N)
 // and [3N, 4N).
 #include <cuda_bf16.h>
@@ -75,11 +78,18 @@ enum : uint32_t {
 
 template <int N>
 struct KrCfg {
-  static_assert(N == 16 || N == 32, "query columns per unit: 16 or 32");
+  static_assert(N == 16, "query columns per unit: 16");
   static constexpr int kRowBytes = N * 128;                  // one 64-column block of N rows
   static constexpr int kQBytes = 2 * kRowBytes;              // Q: N rows x 128 (two blocks)
   static constexpr int kPBytes = 2 * kRowBytes;              // P^T: N rows x 128 keys (two blocks)
+  // Six 32 KB stages. The count must be even: K_j sits at ring position 2j and V_j at 2j + 1, so with an even count
+  // the K tiles only ever use the even stages and the V tiles the odd ones, and each stage has a
+  // single producer (warp 0 or 2) and a single consumer (the S^T or the P V issuer) taking its
+  // positions in order. With an odd count a stage would carry K and V tiles in turn, and the S^T
+  // issuer, which runs ahead of the P V stream, could take a phase of a stage's full barrier that
+  // belongs to a V tile not yet landed (parity waits tell phases apart only one phase deep).
   static constexpr int kStages = 6;
+  static_assert(kStages % 2 == 0, "K and V tiles must not share ring stages");
   static constexpr int kSmemBytes = 1024 + 2 * kQBytes + 2 * kPBytes + kStages * kStageBytes;
   static constexpr uint32_t kTmemCols = 4 * N;               // 64 or 128: a power of two >= 32
 };
@@ -131,19 +141,6 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) 
   }
 }
 
-// Non-blocking test of an mbarrier phase (no suspension, no time limit: the caller waits later).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Start-address step (16-byte units) of K step kk (16 elements) in a 128-byte-swizzled K-major
 // operand whose 64-column blocks are block_bytes apart: 32 bytes inside a swizzle row, the next
 // block every four steps.
@@ -151,13 +148,12 @@ __device__ __forceinline__ uint64_t kmajor_step(int kk, int block_bytes) {
   return (uint64_t)((kk >> 2) * (block_bytes >> 4) + (kk & 3) * 2);
 }
 
-// N: query columns of the MMAs (16 or 32); R: columns the softmax computes (4, 8, 16 or 32; at
-// least every unit's q_len x group). Columns at or past a unit's rows are masked like keys past
+// N: query columns of the MMAs (16); R: columns the softmax computes (4, 8 or 16; at least every
+// unit's q_len x group). Columns at or past a unit's rows are masked like keys past
 // its end, so the softmax loops have a compile-time trip count and no per-column branches.
-template <int N, int R, int WG>
-__global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __grid_constant__ PrefillParams p) {
+template <int N, int R>
+__global__ void __launch_bounds__(288, 1) decode_tc_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(R <= N, "softmax columns within the MMA's columns");
-  static_assert(WG == 1 || WG == 2, "one or two softmax warpgroups");
   using C = KrCfg<N>;
   constexpr int NS = C::kStages;
 
@@ -171,9 +167,9 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
   __shared__ uint64_t bar_q_full[2], bar_q_empty[2];
   __shared__ uint64_t bar_s_full[2], bar_s_free[2], bar_p_full[2], bar_p_free[2];
   __shared__ uint64_t bar_o_full[2], bar_o_free[2];
-  __shared__ uint64_t bar_x[2 * WG];  // per softmax warpgroup, two phases in turn
+  __shared__ uint64_t bar_x[2];  // the softmax warps' exchanges, two phases in turn
   __shared__ uint64_t bar_u_full[kUnitSlots], bar_u_empty[kUnitSlots];
-  __shared__ uint64_t bar_drain;
+  __shared__ uint64_t bar_drain[2];
   __shared__ uint64_t bar_req;  // the producer asks for the next unit
   __shared__ KrUnit units[kUnitSlots];
   __shared__ int unit_pages[kUnitSlots][32];  // physical ids of a unit's first 32 pages
@@ -193,18 +189,19 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       mbar_init(&bar_q_full[b], 1);
       mbar_init(&bar_q_empty[b], 1);
       mbar_init(&bar_s_full[b], 1);
-      mbar_init(&bar_s_free[b], 128 * WG);
-      mbar_init(&bar_p_full[b], 128 * WG);
+      mbar_init(&bar_s_free[b], 128);
+      mbar_init(&bar_p_full[b], 128);
       mbar_init(&bar_p_free[b], 1);
       mbar_init(&bar_o_full[b], 1);
-      mbar_init(&bar_o_free[b], 128 * WG);
+      mbar_init(&bar_o_free[b], 128);
     }
-    for (int b = 0; b < 2 * WG; ++b) mbar_init(&bar_x[b], 4);
+    for (int b = 0; b < 2; ++b) mbar_init(&bar_x[b], 4);
     for (int s = 0; s < kUnitSlots; ++s) {
       mbar_init(&bar_u_full[s], 1);
-      mbar_init(&bar_u_empty[s], 3 + 4 * WG);  // producers, issuer and the softmax warps
+      mbar_init(&bar_u_empty[s], 8);  // two producers, two issuers, four softmax warps
     }
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain[0], 1);
+    mbar_init(&bar_drain[1], 1);
     mbar_init(&bar_req, 1);
     fence_mbar_init();
   }
@@ -358,50 +355,57 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       }
     }
   } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    const uint32_t idesc_s = make_idesc_bf16(128, N, false);   // S^T = K . Q^T
-    const uint32_t idesc_o = make_idesc_bf16_amn(128, N);      // O^T += V^T . P^T (V read MN-major)
+    // ================================================================ S^T issuer
+    const uint32_t idesc_s = make_idesc_bf16(128, N, false);  // S^T = K . Q^T
     uint32_t kv_it = 0, t = 0;  // ring position and key tiles of this CTA so far
     for (int r = 0;; ++r) {
       KrUnit x;
       if (!take_unit(r, x)) break;
-      const int qb = r & 1, ob = r & 1;
-      const uint32_t tO = tmem + 2 * N + ob * N;
-      if (lane == 0) mbar_wait(&bar_q_full[qb], (r >> 1) & 1, abort, p.status, kSiteKrQ);
-      const uint64_t dq = make_sdesc_sw128(smem_u32(sQ + qb * C::kQBytes), 16, 1024);
-      // S^T of key tile j into S buffer (t + j) & 1, once the softmax has read that buffer's
-      // previous scores (lane 0)
-      auto issue_s = [&](int j) {
-        const uint32_t tt = t + j, sb = tt & 1;
-        const uint32_t ki = kv_it + 2 * j;
-        const int ks = ki % NS;
-        mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteKrFull);
-        if (tt >= 2) mbar_wait(&bar_s_free[sb], ((tt >> 1) - 1) & 1, abort, p.status, kSiteKrSFree);
-        tc_fence_after();
-        const uint64_t dk = make_sdesc_sw128(smem_u32(sKV + ks * kStageBytes), 16, 1024);
+      const int qb = r & 1;
+      if (lane == 0) {
+        mbar_wait(&bar_q_full[qb], (r >> 1) & 1, abort, p.status, kSiteKrQ);
+        const uint64_t dq = make_sdesc_sw128(smem_u32(sQ + qb * C::kQBytes), 16, 1024);
+        // S^T of key tile j into S buffer (t + j) & 1, once the softmax has read that buffer's
+        // previous scores
+        for (int j = 0; j < x.ntiles; ++j) {
+          const uint32_t tt = t + j, sb = tt & 1;
+          const uint32_t ki = kv_it + 2 * j;
+          const int ks = ki % NS;
+          mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteKrFull);
+          if (tt >= 2) mbar_wait(&bar_s_free[sb], ((tt >> 1) - 1) & 1, abort, p.status, kSiteKrSFree);
+          tc_fence_after();
+          const uint64_t dk = make_sdesc_sw128(smem_u32(sKV + ks * kStageBytes), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kHd / 16; ++kk)
-          mma_ss(tmem + sb * N, dk + kmajor_step(kk, kBlockBytes), dq + kmajor_step(kk, C::kRowBytes), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(&bar_s_full[sb]);
-        mma_commit(&bar_empty[ks]);
-        if (j == x.ntiles - 1) mma_commit(&bar_q_empty[qb]);  // the unit's last read of Q
-      };
-      if (lane == 0 && x.ntiles > 0) issue_s(0);
+          for (int kk = 0; kk < kHd / 16; ++kk)
+            mma_ss(tmem + sb * N, dk + kmajor_step(kk, kBlockBytes), dq + kmajor_step(kk, C::kRowBytes), idesc_s,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(&bar_s_full[sb]);
+          mma_commit(&bar_empty[ks]);
+        }
+        mma_commit(&bar_q_empty[qb]);  // the unit's last read of Q (at once when it has no keys)
+      }
+      __syncwarp();
+      t += x.ntiles;
+      kv_it += 2 * x.ntiles;
+    }
+    // drain: every MMA issued has completed before TMEM is released
+    if (lane == 0) {
+      mma_commit(&bar_drain[0]);
+      int no_abort = 0;
+      mbar_wait(&bar_drain[0], 0, &no_abort, p.status, kSiteKrDrain);
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ================================================================ P V issuer
+    const uint32_t idesc_o = make_idesc_bf16_amn(128, N);  // O^T += V^T . P^T (V read MN-major)
+    uint32_t kv_it = 0, t = 0;
+    for (int r = 0;; ++r) {
+      KrUnit x;
+      if (!take_unit(r, x)) break;
+      const int ob = r & 1;
+      const uint32_t tO = tmem + 2 * N + ob * N;
       for (int j = 0; j < x.ntiles; ++j) {
         const uint32_t tt = t + j, sb = tt & 1;
-        // S^T of the next key tile goes first when its keys are already in (the ring runs ahead
-        // of the tensor core: S^T then overlaps this tile's softmax); otherwise P V goes first, so
-        // that V's stage is released as soon as the softmax is done
-        bool s_next = false;
-        if (lane == 0 && j + 1 < x.ntiles) {
-          const uint32_t kn = kv_it + 2 * (j + 1), tn = tt + 1;
-          if (mbar_test(&bar_full[kn % NS], (kn / NS) & 1) &&
-              (tn < 2 || mbar_test(&bar_s_free[tn & 1], ((tn >> 1) - 1) & 1))) {
-            issue_s(j + 1);
-            s_next = true;
-          }
-        }
         const uint32_t vi = kv_it + 2 * j + 1;
         const int vs = vi % NS;
         if (lane == 0) mbar_wait(&bar_full[vs], (vi / NS) & 1, abort, p.status, kSiteKrFull);
@@ -436,34 +440,25 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
                    (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar_p_free[sb]);
           mma_commit(&bar_empty[vs]);
-          if (!s_next && j + 1 < x.ntiles) issue_s(j + 1);
         }
         __syncwarp();
       }
       if (lane == 0) {
-        if (x.ntiles == 0) {
-          mma_commit(&bar_q_empty[qb]);
-          if (r >= 2) mbar_wait(&bar_o_free[ob], ((r >> 1) - 1) & 1, abort, p.status, kSiteKrOFree);
-        }
+        if (x.ntiles == 0 && r >= 2) mbar_wait(&bar_o_free[ob], ((r >> 1) - 1) & 1, abort, p.status, kSiteKrOFree);
         mma_commit(&bar_o_full[ob]);
       }
       __syncwarp();
       t += x.ntiles;
       kv_it += 2 * x.ntiles;
     }
-    // drain: every MMA issued has completed before TMEM is released
     if (lane == 0) {
-      mma_commit(&bar_drain);
+      mma_commit(&bar_drain[1]);
       int no_abort = 0;
-      mbar_wait(&bar_drain, 0, &no_abort, p.status, kSiteKrDrain);
+      mbar_wait(&bar_drain[1], 0, &no_abort, p.status, kSiteKrDrain);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 5) {
     // ================================================================ softmax
-    // with two warpgroups (warps 4-7 and 8-11) each computes half of the columns for every key
-    constexpr int RC = R / WG;                         // columns of this warpgroup
-    const int wg = (warp - 4) >> 2;
-    const int cb = wg * RC;                            // its first column
     const int w = warp & 3;                            // TMEM lane quarter
     const int i = w * 32 + lane;                       // key row of a tile; O^T row d in the epilogue
     const uint32_t lane_off = (uint32_t)(w * 32) << 16;
@@ -475,9 +470,9 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       const int rows = x.q_len * G;  // live columns: column c is token c / G, head hk G + c % G
       const int ob = r & 1;
       const int off = x.kv_len - x.q_len;  // bottom-right causal alignment
-      float m[RC], l[RC];
+      float m[R], l[R];
 #pragma unroll
-      for (int c = 0; c < RC; ++c) {
+      for (int c = 0; c < R; ++c) {
         m[c] = -INFINITY;
         l[c] = 0.f;
       }
@@ -486,8 +481,8 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
         mbar_wait(&bar_s_full[sb], (t >> 1) & 1, abort, p.status, kSiteKrS);
         __syncwarp();
         tc_fence_after();
-        uint32_t sr[RC];
-        tmem_ld_cols<RC>(tmem + sb * N + cb + lane_off, sr);
+        uint32_t sr[R];
+        tmem_ld_cols<R>(tmem + sb * N + lane_off, sr);
         tc_fence_before();
         mbar_arrive(&bar_s_free[sb]);
         // This thread's key counts for the columns in [lo, hi): none past the keys; under causal
@@ -504,20 +499,20 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
         // Does any of this thread's scores exceed the running maximum by more than the threshold?
         // The four warps' answers are exchanged; only then are the exact column maxima gathered.
         float* xr = &xred[xc & 1][0][0];
-        uint64_t* bx = &bar_x[wg * 2];
+        uint64_t* bx = bar_x;
         bool up = false;
 #pragma unroll
-        for (int c = 0; c < RC; ++c) {
-          const float s = (cb + c >= lo && cb + c < hi) ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+        for (int c = 0; c < R; ++c) {
+          const float s = (c >= lo && c < hi) ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
           sr[c] = __float_as_uint(s);
           up |= s > m[c] + kKrRescaleThreshold;
         }
         up = __any_sync(0xffffffffu, up);
-        if (lane == 0) xr[cb * 4 + w] = up ? 1.f : 0.f;
+        if (lane == 0) xr[w] = up ? 1.f : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&bx[xc & 1]);
         mbar_wait(&bx[xc & 1], (xc >> 1) & 1, abort, p.status, kSiteKrX);
-        const float4 votes = *reinterpret_cast<const float4*>(xr + cb * 4);
+        const float4 votes = *reinterpret_cast<const float4*>(xr);
         ++xc;
         if ((votes.x + votes.y) + (votes.z + votes.w) > 0.f) {
           // rare (the first tile of a unit, or a score far above the running maximum; the same
@@ -526,18 +521,18 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
           // previous tile's P V is done, the columns of O^T
           float* xm = &xred[xc & 1][0][0];
 #pragma unroll
-          for (int c = 0; c < RC; ++c) {
+          for (int c = 0; c < R; ++c) {
             const float tmax = warp_max_f32(__uint_as_float(sr[c]));
-            if (lane == 0) xm[(cb + c) * 4 + w] = tmax;
+            if (lane == 0) xm[c * 4 + w] = tmax;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bx[xc & 1]);
           mbar_wait(&bx[xc & 1], (xc >> 1) & 1, abort, p.status, kSiteKrX);
           ++xc;
-          float alpha[RC];
+          float alpha[R];
 #pragma unroll
-          for (int c = 0; c < RC; ++c) {
-            const float4 v = *reinterpret_cast<const float4*>(xm + (cb + c) * 4);
+          for (int c = 0; c < R; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(xm + c * 4);
             const float mt = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
             const bool raise = mt > m[c] + kKrRescaleThreshold;
             alpha[c] = raise ? ex2(m[c] - mt) : 1.f;  // 0 while m is -inf
@@ -549,12 +544,12 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
             mbar_wait(&bar_p_free[tp & 1], (tp >> 1) & 1, abort, p.status, kSiteKrPFree);
             __syncwarp();
             tc_fence_after();
-            const uint32_t tO = tmem + 2 * N + ob * N + cb + lane_off;
-            uint32_t o[RC];
-            tmem_ld_cols<RC>(tO, o);
+            const uint32_t tO = tmem + 2 * N + ob * N + lane_off;
+            uint32_t o[R];
+            tmem_ld_cols<R>(tO, o);
 #pragma unroll
-            for (int c = 0; c < RC; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c]);
-            tmem_st_cols<RC>(tO, o);
+            for (int c = 0; c < R; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c]);
+            tmem_st_cols<R>(tO, o);
             tmem_st_wait();
           }
         }
@@ -563,10 +558,10 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
         uint8_t* prow = sP + sb * C::kPBytes + (i >> 6) * C::kRowBytes + (i & 7) * 2;
         const int ch = (i & 63) >> 3;
 #pragma unroll
-        for (int c = 0; c < RC; ++c) {
+        for (int c = 0; c < R; ++c) {
           const float e = ex2(__uint_as_float(sr[c]) - (m[c] == -INFINITY ? 0.f : m[c]));
           l[c] += e;
-          const int row = cb + c;
+          const int row = c;
           *reinterpret_cast<__nv_bfloat16*>(prow + row * 128 + ((ch ^ (row & 7)) << 4)) = __float2bfloat16_rn(e);
         }
         fence_proxy_async_smem();
@@ -576,32 +571,32 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
       // ------------------------------------------------------------ epilogue
       // l per column over the 128 key rows: a warp sum, then the four warps' sums
       float* xr = &xred[xc & 1][0][0];
-      uint64_t* bx = &bar_x[wg * 2];
+      uint64_t* bx = bar_x;
 #pragma unroll
-      for (int c = 0; c < RC; ++c) {
+      for (int c = 0; c < R; ++c) {
         float v = l[c];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) xr[(cb + c) * 4 + w] = v;
+        if (lane == 0) xr[c * 4 + w] = v;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bx[xc & 1]);
       mbar_wait(&bx[xc & 1], (xc >> 1) & 1, abort, p.status, kSiteKrX);
       ++xc;
 #pragma unroll
-      for (int c = 0; c < RC; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(xr + (cb + c) * 4);
+      for (int c = 0; c < R; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(xr + c * 4);
         l[c] = (v.x + v.y) + (v.z + v.w);
       }
       mbar_wait(&bar_o_full[ob], (r >> 1) & 1, abort, p.status, kSiteKrO);
       __syncwarp();
       tc_fence_after();
-      uint32_t orr[RC];
+      uint32_t orr[R];
       if (x.ntiles > 0) {
-        tmem_ld_cols<RC>(tmem + 2 * N + ob * N + cb + lane_off, orr);
+        tmem_ld_cols<R>(tmem + 2 * N + ob * N + lane_off, orr);
       } else {
 #pragma unroll
-        for (int c = 0; c < RC; ++c) orr[c] = 0u;
+        for (int c = 0; c < R; ++c) orr[c] = 0u;
       }
       tc_fence_before();
       mbar_arrive(&bar_o_free[ob]);  // the MMA may now overwrite this O^T buffer (unit r + 2)
@@ -614,11 +609,11 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
         lse_out = p.lse_part;
         row_base = (int64_t)x.split * p.total_q * p.Hq;
       }
-      int tq = cb / G, g = cb - (cb / G) * G;  // token and head of column cb
+      int tq = 0, g = 0;  // token and head of column c
 #pragma unroll
-      for (int c = 0; c < RC; ++c) {
+      for (int c = 0; c < R; ++c) {
         const int64_t tok = x.tok0 + tq;
-        if (cb + c < rows && tok < p.total_q) {
+        if (c < rows && tok < p.total_q) {
           const int64_t orow = row_base + tok * p.Hq + x.hk * G + g;
           const float inv = l[c] > 0.f ? 1.f / l[c] : 0.f;
           const float o = __uint_as_float(orr[c]) * inv;
@@ -627,7 +622,7 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
           } else {
             reinterpret_cast<__nv_bfloat16*>(p.o)[orow * kHd + i] = __float2bfloat16_rn(o);
           }
-          if (i == cb + c && lse_out != nullptr)
+          if (i == c && lse_out != nullptr)
             lse_out[orow] = l[c] > 0.f ? (m[c] + __log2f(l[c])) * kKrLn2 : -INFINITY;
         }
         if (++g == G) {
@@ -648,9 +643,8 @@ __global__ void __launch_bounds__(128 + 128 * WG, 1) decode_tc_kernel(const __gr
 
 template <int R>
 cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
-  constexpr int N = R < 16 ? 16 : R;
-  constexpr int WG = R == 32 ? 2 : 1;  // 32 columns: two softmax warpgroups of 16
-  auto kern = decode_tc_kernel<N, R, WG>;
+  constexpr int N = 16;
+  auto kern = decode_tc_kernel<N, R>;
   static std::atomic<unsigned> configured_mask{0u};  // one bit per device ordinal below 32
   int dev = 0;
   cudaGetDevice(&dev);
@@ -659,7 +653,7 @@ cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t
     if (e != cudaSuccess) return e;
     if (dev < 32) configured_mask.fetch_or(1u << dev, std::memory_order_release);
   }
-  kern<<<grid, 128 + 128 * WG, KrCfg<N>::kSmemBytes, stream>>>(p);
+  kern<<<grid, 288, KrCfg<N>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -668,7 +662,7 @@ cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t
 int decode_tc_columns(int max_q_len, int group, int d, int max_rows) {
   if (d != kHd || max_q_len < 1 || group < 1) return 0;
   const long long rows = (long long)max_q_len * group;
-  if (rows > max_rows || rows > 32) return 0;
+  if (rows > max_rows || rows > 16) return 0;
   int r = 4;
   while (r < rows) r *= 2;
   return r;
@@ -685,7 +679,6 @@ cudaError_t launch_decode_tc(const PrefillParams& p, int columns, int sm_count, 
     case 4: return launch_decode_tc_impl<4>(p, grid, stream);
     case 8: return launch_decode_tc_impl<8>(p, grid, stream);
     case 16: return launch_decode_tc_impl<16>(p, grid, stream);
-    case 32: return launch_decode_tc_impl<32>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

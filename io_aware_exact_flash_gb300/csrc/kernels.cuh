@@ -118,11 +118,11 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_plan_paged(const PrefillParams& p, int max_items, int max_kv_tiles, int2* work_list,
                               int* work_count, cudaStream_t stream);
 // Decode / verify with the keys on the MMA's rows (decode_tc.cu): the query columns the softmax
-// computes per unit (4, 8, 16 or 32: the power of two >= max_q_len x group) for batches of at most
-// max_rows (<= 32) query rows per (sequence, kv head) at d = 128, else 0.
+// computes per unit (4, 8 or 16: the power of two >= max_q_len x group) for batches of at most
+// max_rows (<= 16) query rows per (sequence, kv head) at d = 128, else 0.
 int decode_tc_columns(int max_q_len, int group, int d, int max_rows);
 // Plans the batch (p.pack must be 1 for the plan) and runs it on min(units, sm_count) persistent
-// CTAs. p.tm_q's box is {64, group, max(16, columns) / group, 1}.
+// CTAs. p.tm_q's box is {64, group, 16 / group, 1}.
 cudaError_t launch_decode_tc(const PrefillParams& p, int columns, int sm_count, int max_items, int max_kv_tiles,
                              int2* work_list, int* work_count, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H,

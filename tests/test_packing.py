@@ -2,8 +2,7 @@
 cases), so every shape there is checked against the oracle on each path: GQA packing of the
 tensor-core path (a tile's rows = token x head of one kv head's query heads) off, decode batches
 on the split-KV CUDA-core kernel instead of the tensor cores, decode and verify batches on the
-packed prefill kernel instead of the key-row kernel, the key-row kernel also for 17-32 query rows
-per kv head, and the prefill launch modes. The seeded random shapes of test_fuzz.py run
+packed prefill kernel instead of the key-row kernel, and the prefill launch modes. The seeded random shapes of test_fuzz.py run
 under each of them too (the default paths run in the suites themselves)."""
 import os
 import subprocess
@@ -16,9 +15,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("env", [{"FA_PAGED_PACK": "0"}, {"FA_DECODE_TC": "0"}, {"FA_DECODE_KEY_ROWS": "0"},
-                                 {"FA_DECODE_KEY_ROWS": "2"}],
-                         ids=["never_pack", "decode_on_cuda_cores", "decode_on_packed_tiles", "key_rows_to_32"])
+@pytest.mark.parametrize("env", [{"FA_PAGED_PACK": "0"}, {"FA_DECODE_TC": "0"}, {"FA_DECODE_KEY_ROWS": "0"}],
+                         ids=["never_pack", "decode_on_cuda_cores", "decode_on_packed_tiles"])
 def test_paged_parity_with_forced_paths(env):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-k", "not full_size",
                         "-p", "no:cacheprovider", "tests/test_parity_paged.py", "tests/test_cascade.py",

@@ -190,6 +190,24 @@ def test_multi_token_verify(d, Hq, Hkv):
     compare(o, o_ref, lse, lse_ref, f"verify d={d} Hq={Hq} Hkv={Hkv}", vabs=va_ref)
 
 
+@pytest.mark.parametrize("Hq,Hkv,q_lens,page_size,splits", [
+    (32, 8, [1, 4, 2, 3, 1, 4, 2, 1], 16, 0),    # verify of <= 4 tokens, group 4: 16 query columns
+    (32, 8, [2, 1, 2, 2, 1, 1, 2, 2], 64, 3),    # 8 columns, key splits, 64-row pages
+    (32, 2, [1] * 8, 16, 0),                     # decode, group 16: 16 columns
+    (12, 4, [1, 4, 5, 2, 3, 1, 5, 4], 32, 2),    # group 3 (not a power of two), up to 15 rows
+    (8, 8, [1, 2, 4, 3, 1, 4, 2, 1], 128, 0),    # MHA verify, 128-row pages
+])
+def test_key_row_kernel_shapes(Hq, Hkv, q_lens, page_size, splits):
+    """Batches of at most 16 query rows per kv head, which run on the key-row kernel: every
+    column count it compiles (4, 8, 16), groups that do and do not divide 16, causal verify rows,
+    key splits and page sizes, against the oracle."""
+    lengths = [5, 16, 130, 300, 1000, 2049, 777, 4100]
+    t = build_case(lengths, Hq, Hkv, 128, page_size, False, 91 + Hq + page_size, q_lens=q_lens, extra_pages=2)
+    o, lse = run_paged(t, True, 1 / math.sqrt(128), num_splits=splits)
+    o_ref, lse_ref, va_ref = oracle_paged(t, True, 1 / math.sqrt(128))
+    compare(o, o_ref, lse, lse_ref, f"key rows Hq={Hq} Hkv={Hkv} ps={page_size}", vabs=va_ref)
+
+
 @pytest.mark.parametrize("name", ["mixed_paged_64seq_512_8192_hq32_hkv8_d128_p16",
                                   "verify_paged_128seq_q2_8_kv1024_16384_hq32_hkv8_d128_p16"])
 def test_mixed_and_verify_workloads_full_size(name):
