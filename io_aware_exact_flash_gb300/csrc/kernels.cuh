@@ -12,7 +12,7 @@ namespace fa {
 constexpr int kBM = 128;   // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;   // keys per tile
 constexpr int kQTiles = 2; // query tiles per CTA (ping-pong between the two softmax warpgroups)
-constexpr int kPrefillThreads = 384;  // warp 0 TMA, warps 1-2 MMA, warp 3 spare, 4-11 softmax
+constexpr int kPrefillThreads = 384;  // warps 0 (and 3, paged) TMA, warps 1-2 MMA, 4-11 softmax
 // Registers per thread after the prefill CTA's split: warpgroup 0 (TMA, MMA, spare warps) drops
 // to kRegsControl, the two softmax warpgroups rise to kRegsSoftmax. The sum stays within the
 // 384 x 168 registers the CTA launches with (the launcher checks the compiled count).

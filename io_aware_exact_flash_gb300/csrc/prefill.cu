@@ -18,7 +18,7 @@
 //   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into a ring of stages
 //   warp 1      TMEM owner; one lane issues every tcgen05.mma of query tile 0
 //   warp 2      one lane issues every tcgen05.mma of query tile 1
-//   warp 3      idle
+//   warp 3      paged layout: second TMA producer (the V tiles; warp 0 then loads Q and K); dense: idle
 //   warps 4-7   softmax warpgroup 0 -> query tile 0 (rows 0..127 of the CTA's 256)
 //   warps 8-11  softmax warpgroup 1 -> query tile 1 (rows 128..255)
 // The two warpgroups ping-pong: while one computes its softmax the tensor core runs the other's
@@ -261,7 +261,7 @@ struct TakeOver {
   uint4 resp[2];
   uint64_t full[2], empty[2];
 };
-constexpr int kUnitWalkers = 11;  // warps 0-2 and 4-11
+constexpr int kUnitWalkers = 11;  // warps 0-2 and 4-11 (and warp 3 on the paged layout)
 
 // Which units a CTA runs, in the same sequence in every warp. A persistent launch walks the snake
 // order of unit_of_round. Otherwise a CTA runs work item blockIdx.x; with TAKE, once its item is
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     mbar_init(&bar_turn[1], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&take.full[s], 1);
-      mbar_init(&take.empty[s], kUnitWalkers);
+      mbar_init(&take.empty[s], PAGED ? kUnitWalkers + 1 : kUnitWalkers);
     }
     fence_mbar_init();
   }
@@ -364,9 +364,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   const uint32_t tmem = tmem_base_sh;
   volatile int* abort = &abort_flag;
 
-  if (warp == 0) {
+  if (warp == 0 || (PAGED && warp == 3)) {
     regs_dec<kRegsControl>();
-    // ================================================================ TMA producer
+    // ================================================================ TMA producer(s)
+    // Paged: warp 0 loads Q and the K tiles, warp 3 the V tiles. With 16-row pages a tile is 16
+    // tensor boxes of 2 KB per 64-column block, more than one warp's lanes issue in time for
+    // memory-bound batches (multi-token verify). Both walk every unit and every ring position.
+    const bool v_warp = PAGED && warp == 3;
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       if (u < 0) break;
       Unit w;
       unit_at<PAGED>(p, u, w);
-      if (lane == 0) {
+      if (lane == 0 && !v_warp) {
         // the previous unit's last Q K^T must have read the Q tiles before they are replaced
         if (r > 0) mbar_wait(&bar_q_empty, (r - 1) & 1, abort, p.status, kSiteProducerEmpty);
         int n_active = 0;
@@ -401,21 +405,31 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         }
       }
       __syncwarp();
-      // paged: lane l < 128 / page_size holds the physical id of page l of the current key tile;
-      // the ids of the next tile are fetched right after this tile's K boxes are issued, so the
-      // page-table read is off the path to the next TMA
+      // paged: page ids come 32 at a time, lane l holding the unit's page 32 b + l of batch b; the
+      // next batch is read while the current one is used, so no page-table read is waited for
+      // (past the keys the id is past the pool, where TMA reads zeros)
       const int ppt = PAGED ? kBN / p.page_size : 0;  // pages per key tile
-      auto page_id = [&](int tile) {
-        const int lp = tile * ppt + lane;  // logical page of this sequence
-        return lp * p.page_size < w.kv_len ? p.page_table[(int64_t)w.seq * p.max_pages_per_seq + lp]
-                                           : p.num_pages;  // past the pool: TMA fills zeros
+      const int n_pages = w.nmax * ppt;                // pages of the unit's key range
+      auto page_batch = [&](int b) {
+        const int lp = w.kv_t0 * ppt + b * 32 + lane;  // logical page of this sequence
+        return lp * p.page_size < w.kv_len ? p.page_table[(int64_t)w.seq * p.max_pages_per_seq + lp] : p.num_pages;
       };
-      int phys_cur = 0, phys_next = 0;
-      if (PAGED && lane < ppt && w.nmax > 0) phys_cur = page_id(w.kv_t0);
+      int pages_cur = 0, pages_next = 0, phys = 0;
+      if (PAGED && n_pages > 0) pages_cur = page_batch(0);
+      if (PAGED && n_pages > 32) pages_next = page_batch(1);
       for (int idx = 0; idx < 2 * w.nmax; ++idx, ++kv_it) {
         const int j = idx >> 1;
         const bool is_v = idx & 1;
         const int stage = kv_it % NS;
+        if (PAGED && !is_v) {
+          const int pj = j * ppt;  // the tile's first page within the unit
+          if (j > 0 && (pj & 31) == 0) {
+            pages_cur = pages_next;
+            if (pj + 32 < n_pages) pages_next = page_batch((pj >> 5) + 1);
+          }
+          phys = __shfl_sync(0xffffffffu, pages_cur, (pj & 31) + (lane < ppt ? lane : 0));
+        }
+        if (PAGED && is_v != v_warp) continue;  // the other producer's stage
         if (lane == 0) mbar_wait(&bar_empty[stage], ((kv_it / NS) & 1) ^ 1, abort, p.status, kSiteProducerEmpty);
         __syncwarp();
         uint8_t* dst = sKV + stage * TB;
@@ -434,12 +448,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub)
               tma_load_4d_hint(dst + sub * C::kSubBytes + lane * p.page_size * 128, tm, &bar_full[stage],
-                               sub * 64, w.hk, 0, phys_cur, kv_policy);
-            if (!is_v) {
-              phys_next = page_id(w.kv_t0 + j + 1);
-            } else {
-              phys_cur = phys_next;
-            }
+                               sub * 64, w.hk, 0, phys, kv_policy);
           }
         }
         __syncwarp();
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
       // The item's last unit is loaded: ask for the next item now, about a ring's depth of key
       // tiles before the walkers need it. One request is in flight at a time, and none follows a
       // failed one (the walk ends there).
-      if (TAKE && cur.item_done()) {
+      if (TAKE && cur.item_done() && !v_warp) {
         int issued = 0;
         if (lane == 0 && !*abort) {
           const uint32_t s = requests & 1;  // the slot's previous response must have been read
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     }
     __syncwarp();
   } else if (warp == 3) {
-    regs_dec<kRegsControl>();
+    regs_dec<kRegsControl>();  // dense layout: idle
   } else if (warp >= 4) {
     regs_inc<kRegsSoftmax>();
     // ================================================================ softmax warpgroups
