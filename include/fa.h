@@ -22,7 +22,8 @@
  *  - Supported head dims: d = 64 and d = 128. Every pointer must be 16-byte aligned.
  *  - Memory: the caller owns all device memory (inputs, outputs, workspace). The library never
  *    allocates or frees device memory. Its only global state is one device status word per GPU
- *    (see fa_get_device_status) and a cached driver entry point.
+ *    (see fa_get_device_status), a cached driver entry point, and for fa_cascade_fwd one stream
+ *    and two events per calling host thread and GPU (created on first use, never freed).
  *  - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
  *    FA_OK means validated and enqueued. Calls on different streams may run concurrently as
  *    long as they do not share an output or a workspace.
@@ -147,9 +148,11 @@ fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_
  * Result (o bf16 [total_q, Hq, d], lse fp32 [total_q, Hq] or NULL): exactly fa_paged_fwd over the
  * concatenated keys prefix(g) ++ suffix(s) of every sequence. Every query row sees the whole
  * prefix; with causal != 0 the suffix is masked bottom-right, which needs q_len(s) <= kv_lens[s]
- * (the query tokens lie in the suffix). Both passes run the same kernels as fa_paged_fwd (decode
- * when the pass's max query length is 1, else the tensor-core kernel) with fp32 outputs, then one
- * merge: three launches plus planning, in order on `stream`.
+ * (the query tokens lie in the suffix). Both passes run the same kernels as fa_paged_fwd with
+ * fp32 outputs, then one merge. The suffix pass runs on a second stream of the library's (one per
+ * calling host thread and GPU, created on first use), forked from `stream` with an event before
+ * the prefix pass and joined back into it before the merge, so the two passes share the GPU: the
+ * call is ordered on `stream` like any other (and can be captured in a CUDA graph from it).
  *   max_group_q_len / max_q_len: host-side bounds of the query rows per group / per sequence.
  *   workspace: at least fa_cascade_workspace_bytes(...) bytes, 256-byte aligned.
  * Errors as for fa_paged_fwd; also FA_ERR_INVALID_ARG when num_groups > num_seqs.
