@@ -172,14 +172,14 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint6
   }
 }
 
-// O (+)= P V for one tile: P (bf16 pairs) from TMEM as A, V as the MN-major B operand; a K step
-// of 16 keys is 16 rows of 128 bytes (2048 bytes) in each 64-column block of d, and P's 16 keys
-// are 8 TMEM columns.
-template <int D>
+// O (+)= P V over keys [16 K0, 16 K1) of one tile: P (bf16 pairs) from TMEM as A, V as the
+// MN-major B operand; a K step of 16 keys is 16 rows of 128 bytes (2048 bytes) in each 64-column
+// block of d, and P's 16 keys are 8 TMEM columns.
+template <int D, int K0 = 0, int K1 = kBN / 16>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t idesc,
                                          uint32_t accumulate) {
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk)
+  for (int kk = K0; kk < K1; ++kk)
     mma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)kk * (2048 >> 4), idesc, kk > 0 ? 1u : accumulate);
 }
 
@@ -206,6 +206,29 @@ __device__ __forceinline__ uint64_t softmax_chunks(const uint32_t* sr, float sl2
     tmem_st16(tS + cc * 16, pk);
   }
   return add_f32x2(add_f32x2(ls4[0], ls4[1]), add_f32x2(ls4[2], ls4[3]));
+}
+
+// O rescale by alpha when a row's running maximum moved (rare: a loop that is not unrolled keeps
+// the code small). Runs before the tile's P is released to the MMA: P V of the previous tile is
+// complete, because the commit that signalled this tile's S was issued after it.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tO, bool any_need, float alpha) {
+  if (!any_need) return;
+  const uint64_t a2 = f32x2(alpha, alpha);
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t orr[32];
+    tmem_ld32(tO + cc * 32, orr);
+    tmem_ld_wait(orr);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float a, b;
+      split_f32x2(mul_f32x2(f32x2(u2f(orr[2 * i]), u2f(orr[2 * i + 1])), a2), a, b);
+      orr[2 * i] = f2u(a);
+      orr[2 * i + 1] = f2u(b);
+    }
+    tmem_st32(tO + cc * 32, orr);
+  }
 }
 
 // Row max of 32-column chunks [C0, C0 + NC): four independent chains of three-input max.
@@ -313,6 +336,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   using C = Cfg<D>;
   constexpr int NS = C::kStages;
   constexpr int TB = C::kTileBytes;
+  // d = 64 releases each tile's P to the MMA in two halves (measured faster there; at d = 128 one
+  // hand-off per tile is faster)
+  constexpr bool kHalfP = D == 64;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -320,7 +346,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   uint8_t* sKV = smem + kQTiles * TB;  // NS stages
 
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_full[NS], bar_empty[NS];
-  __shared__ uint64_t bar_s[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_o_free[kQTiles], bar_drain[kQTiles];
+  __shared__ uint64_t bar_s[kQTiles], bar_ph[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_o_free[kQTiles],
+      bar_drain[kQTiles];
   __shared__ uint64_t bar_turn[2];
   __shared__ alignas(16) TakeOver take;
   __shared__ uint32_t tmem_base_sh;
@@ -337,6 +364,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 #pragma unroll
     for (int g = 0; g < kQTiles; ++g) {
       mbar_init(&bar_s[g], 1);
+      mbar_init(&bar_ph[g], 4 * 32);
       mbar_init(&bar_p[g], 4 * 32);
       mbar_init(&bar_o[g], 1);
       mbar_init(&bar_o_free[g], 4 * 32);
@@ -574,13 +602,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
               __syncwarp();
             }
             if (lane == 0) {
-              mbar_wait(&bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
+              // At d = 64, P arrives in two halves (keys 0-63, then 64-127): the first half's P V
+              // is issued while the softmax still computes the second half.
+              mbar_wait(kHalfP ? &bar_ph[g] : &bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
               // the first P V of a unit overwrites O: the previous unit's O must have been read
               if (j == 0 && ounits > 0) mbar_wait(&bar_o_free[g], (ounits - 1) & 1, abort, p.status, kSiteMmaP);
               if (j + 1 < nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
               if (j < nkv_both) take_turn();
               tc_fence_after();
-              issue_pv<D>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
+              if constexpr (kHalfP) {
+                issue_pv<D, 0, kBN / 32>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
+                mbar_wait(&bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
+                tc_fence_after();
+                issue_pv<D, kBN / 32, kBN / 16>(tO, tS, dv + vs * (TB >> 4), idesc_pv, 1u);
+              } else {
+                issue_pv<D>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
+              }
               if (j + 1 < nkv) issue_qk<D>(tS, dq, dk + ks * (TB >> 4), idesc_s);
               if (j < nkv_both) pass_turn();
               if (j == nkv - 1) {
@@ -649,6 +686,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         mbar_wait(&bar_s[g], tcnt & 1, abort, p.status, kSiteSoftmaxS);
         __syncwarp();  // lanes leave the wait at different times; tcgen05.ld is warp-collective
         if (!live) {
+          if constexpr (kHalfP) mbar_arrive(&bar_ph[g]);
           mbar_arrive(&bar_p[g]);
           continue;
         }
@@ -683,29 +721,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         const bool need = m_tile > m_run + kRescaleThreshold;
         const float alpha = need ? ex2(m_run - m_tile) : 1.f;  // 0 while m_run is -inf
         if (need) m_run = m_tile;
+        const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
         float la, lb;
-        split_f32x2(softmax_chunks<0, 4>(sr, sl2, m_run == -INFINITY ? 0.f : -m_run, tS), la, lb);
-        l_run = fmaf(l_run, alpha, la + lb);
-        // O rescale (after P is written, so S no longer occupies registers): P V of the previous
-        // tile is complete, because the commit that signalled this tile's S was issued after it.
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // rare: a loop that is not unrolled keeps the code small
-          const uint64_t a2 = f32x2(alpha, alpha);
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t orr[32];
-            tmem_ld32(tO + cc * 32, orr);
-            tmem_ld_wait(orr);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float a, b;
-              split_f32x2(mul_f32x2(f32x2(u2f(orr[2 * i]), u2f(orr[2 * i + 1])), a2), a, b);
-              orr[2 * i] = f2u(a);
-              orr[2 * i + 1] = f2u(b);
-            }
-            tmem_st32(tO + cc * 32, orr);
-          }
+        if constexpr (kHalfP) {
+          split_f32x2(softmax_chunks<0, 2>(sr, sl2, neg_m, tS), la, lb);
+          rescale_o<D>(tO, j > 0 && __any_sync(0xffffffffu, need), alpha);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bar_ph[g]);  // keys 0-63 of P (and the rescaled O) are in TMEM
+          float lc, ld;
+          split_f32x2(softmax_chunks<2, 2>(sr, sl2, neg_m, tS), lc, ld);
+          la += lc;
+          lb += ld;
+        } else {
+          split_f32x2(softmax_chunks<0, 4>(sr, sl2, neg_m, tS), la, lb);
+          // after P is written, so S no longer occupies registers
+          rescale_o<D>(tO, j > 0 && __any_sync(0xffffffffu, need), alpha);
         }
+        l_run = fmaf(l_run, alpha, la + lb);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar_p[g]);

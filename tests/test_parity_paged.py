@@ -128,6 +128,19 @@ def test_paged_decode_empty_sequence():
         assert np.all(o[1] == 0) and np.all(np.isneginf(lse[1]))
 
 
+def test_key_row_many_key_splits():
+    """The key-row kernel with 16 key splits over sequences of 0 to 5000 keys, so most splits of
+    the short sequences hold no key tile, and verify rows besides decode ones; a second call gives
+    the same bits (the planning state is rebuilt on every call)."""
+    t = build_case([1, 0, 130, 5000, 16, 2049, 700, 3], 32, 8, 128, 16, False, 97, q_lens=[1, 1, 2, 1, 4, 1, 3, 1],
+                   extra_pages=2)
+    o1, lse1 = run_paged(t, True, 1 / math.sqrt(128), num_splits=16)
+    o2, lse2 = run_paged(t, True, 1 / math.sqrt(128), num_splits=16)
+    assert np.array_equal(o1, o2) and np.array_equal(lse1, lse2)
+    o_ref, lse_ref, va_ref = oracle_paged(t, True, 1 / math.sqrt(128))
+    compare(o1, o_ref, lse1, lse_ref, "key rows, 16 key splits", vabs=va_ref)
+
+
 def test_paged_prefill_full_size_sampled():
     """The ragged paged prefill workload (64 sequences, lengths 512..8192) at full size, in the
     benchmark's launch configuration, checked on sampled (token, head) rows."""
