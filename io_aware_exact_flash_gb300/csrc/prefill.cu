@@ -25,7 +25,9 @@
 // P V and next Q K^T (the two MMA issuers take turns to keep that order).
 //
 // TMEM columns: S/P of tile g at [128 g, 128 g + 128) (P, as packed bf16 pairs, overwrites the
-// first 64 columns of S), O of tile g at [256 + g D, 256 + (g+1) D).
+// first 64 columns of S), O of tile g at [256 + g D, 256 + (g+1) D). At d = 64, P of tile g has
+// columns [384 + 64 g, 448 + 64 g) of its own: the issuer then puts a tile's next Q K^T ahead of
+// its P V as soon as the softmax has read S, and the issuers do not take turns.
 #include <cuda_bf16.h>
 #include <atomic>
 #include <cstdlib>
@@ -65,6 +67,8 @@ enum : uint32_t {
   kSiteDrain = 7,
   kSiteMmaTurn = 8,
   kSiteTakeOver = 9,
+  kSiteMmaSFree = 10,
+  kSiteSoftmaxPV = 11,
 };
 
 // One unit of work: a pair of 128-row query tiles of one (sequence, query head), or, with GQA
@@ -172,14 +176,14 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint6
   }
 }
 
-// O (+)= P V over keys [16 K0, 16 K1) of one tile: P (bf16 pairs) from TMEM as A, V as the
-// MN-major B operand; a K step of 16 keys is 16 rows of 128 bytes (2048 bytes) in each 64-column
-// block of d, and P's 16 keys are 8 TMEM columns.
-template <int D, int K0 = 0, int K1 = kBN / 16>
+// O (+)= P V for one tile: P (bf16 pairs) from TMEM as A, V as the MN-major B operand; a K step
+// of 16 keys is 16 rows of 128 bytes (2048 bytes) in each 64-column block of d, and P's 16 keys
+// are 8 TMEM columns.
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t idesc,
                                          uint32_t accumulate) {
 #pragma unroll
-  for (int kk = K0; kk < K1; ++kk)
+  for (int kk = 0; kk < kBN / 16; ++kk)
     mma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)kk * (2048 >> 4), idesc, kk > 0 ? 1u : accumulate);
 }
 
@@ -229,6 +233,22 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, bool any_need, float alph
     }
     tmem_st32(tO + cc * 32, orr);
   }
+}
+
+// Softmax numerators of a whole 128-key score row held in registers, like softmax_chunks, with P
+// left in registers (pk: bf16 pairs) for the caller to store. Returns the row sum as two halves.
+__device__ __forceinline__ uint64_t softmax_regs(const uint32_t* sr, float sl2, float neg_m, uint32_t* pk) {
+  const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
+  uint64_t ls4[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < kBN / 2; ++i) {
+    float x0, x1;
+    split_f32x2(fma_f32x2(f32x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, negm2), x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    ls4[i & 3] = add_f32x2(ls4[i & 3], f32x2(p0, p1));
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+  return add_f32x2(add_f32x2(ls4[0], ls4[1]), add_f32x2(ls4[2], ls4[3]));
 }
 
 // Row max of 32-column chunks [C0, C0 + NC): four independent chains of three-input max.
@@ -336,9 +356,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   using C = Cfg<D>;
   constexpr int NS = C::kStages;
   constexpr int TB = C::kTileBytes;
-  // d = 64 releases each tile's P to the MMA in two halves (measured faster there; at d = 128 one
-  // hand-off per tile is faster)
-  constexpr bool kHalfP = D == 64;
+  // d = 64 leaves 128 TMEM columns free (S 2 x 128 and O 2 x 64 of 512): P gets a region of its
+  // own there instead of overwriting S, so each tile's next Q K^T is issued as soon as the softmax
+  // has read S, ahead of this tile's P V (the next scores are ready when the softmax is)
+  constexpr bool kSepP = D == 64;
+  constexpr uint32_t kColP = 384;  // kSepP: P of query tile g at columns 384 + 64 g (bf16 pairs)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -346,8 +368,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
   uint8_t* sKV = smem + kQTiles * TB;  // NS stages
 
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_full[NS], bar_empty[NS];
-  __shared__ uint64_t bar_s[kQTiles], bar_ph[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_o_free[kQTiles],
-      bar_drain[kQTiles];
+  __shared__ uint64_t bar_s[kQTiles], bar_p[kQTiles], bar_o[kQTiles], bar_o_free[kQTiles], bar_drain[kQTiles];
+  __shared__ uint64_t bar_sfree[kQTiles], bar_pv[kQTiles];  // separate P (d = 64) only
   __shared__ uint64_t bar_turn[2];
   __shared__ alignas(16) TakeOver take;
   __shared__ uint32_t tmem_base_sh;
@@ -364,7 +386,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 #pragma unroll
     for (int g = 0; g < kQTiles; ++g) {
       mbar_init(&bar_s[g], 1);
-      mbar_init(&bar_ph[g], 4 * 32);
+      mbar_init(&bar_sfree[g], 4 * 32);
+      mbar_init(&bar_pv[g], 1);
       mbar_init(&bar_p[g], 4 * 32);
       mbar_init(&bar_o[g], 1);
       mbar_init(&bar_o_free[g], 4 * 32);
@@ -562,12 +585,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           // also when its tile does not read the stage: an issuer can then never arrive twice on
           // one pending phase, because the next fill waits for that phase to complete.
           mbar_wait(&bar_full[ks0], (kv_it / NS) & 1, abort, p.status, kSiteMmaFull);
-          if (nkv_both > 0) take_turn();
+          if (!kSepP && nkv_both > 0) take_turn();
           if (nkv > 0) {
             tc_fence_after();
             issue_qk<D>(tS, dq, dk + ks0 * (TB >> 4), idesc_s);
           }
-          if (nkv_both > 0) pass_turn();
+          if (!kSepP && nkv_both > 0) pass_turn();
           if (nkv > 0) {
             mma_commit(&bar_s[g]);
             if (nkv == 1) mma_commit(&bar_q_empty);  // the unit's last Q K^T of this tile
@@ -578,6 +601,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           const uint32_t vi = kv_it + 2 * j + 1, ki = kv_it + 2 * j + 2;
           const int vs = vi % NS, ks = ki % NS;
           const bool has_next = j + 1 < w.nmax;
+          if constexpr (kSepP) {
+            // the next key tile's Q K^T first: S is free once the softmax has read this tile's
+            if (lane == 0 && has_next) {
+              mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
+              if (j + 1 < nkv) {
+                mbar_wait(&bar_sfree[g], tcnt & 1, abort, p.status, kSiteMmaSFree);
+                tc_fence_after();
+                issue_qk<D>(tS, dq, dk + ks * (TB >> 4), idesc_s);
+                mma_commit(&bar_s[g]);
+                if (j + 2 == nkv) mma_commit(&bar_q_empty);  // the unit's last Q K^T of this tile
+              }
+              mma_commit(&bar_empty[ks]);
+            }
+            __syncwarp();
+          }
           if (lane == 0) mbar_wait(&bar_full[vs], (vi / NS) & 1, abort, p.status, kSiteMmaFull);
           __syncwarp();
           if (j < nkv) {
@@ -601,23 +639,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
               }
               __syncwarp();
             }
-            if (lane == 0) {
-              // At d = 64, P arrives in two halves (keys 0-63, then 64-127): the first half's P V
-              // is issued while the softmax still computes the second half.
-              mbar_wait(kHalfP ? &bar_ph[g] : &bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
+            if (kSepP && lane == 0) {
+              mbar_wait(&bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
+              // the first P V of a unit overwrites O: the previous unit's O must have been read
+              if (j == 0 && ounits > 0) mbar_wait(&bar_o_free[g], (ounits - 1) & 1, abort, p.status, kSiteMmaP);
+              tc_fence_after();
+              issue_pv<D>(tO, tmem + kColP + g * 64, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
+              mma_commit(&bar_pv[g]);  // P and O are free for the next tile's softmax
+              if (j == nkv - 1) {
+                mma_commit(&bar_o[g]);
+                ++ounits;
+              }
+            } else if (lane == 0) {
+              mbar_wait(&bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
               // the first P V of a unit overwrites O: the previous unit's O must have been read
               if (j == 0 && ounits > 0) mbar_wait(&bar_o_free[g], (ounits - 1) & 1, abort, p.status, kSiteMmaP);
               if (j + 1 < nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
               if (j < nkv_both) take_turn();
               tc_fence_after();
-              if constexpr (kHalfP) {
-                issue_pv<D, 0, kBN / 32>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
-                mbar_wait(&bar_p[g], tcnt & 1, abort, p.status, kSiteMmaP);
-                tc_fence_after();
-                issue_pv<D, kBN / 32, kBN / 16>(tO, tS, dv + vs * (TB >> 4), idesc_pv, 1u);
-              } else {
-                issue_pv<D>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
-              }
+              issue_pv<D>(tO, tS, dv + vs * (TB >> 4), idesc_pv, j > 0 ? 1u : 0u);
               if (j + 1 < nkv) issue_qk<D>(tS, dq, dk + ks * (TB >> 4), idesc_s);
               if (j < nkv_both) pass_turn();
               if (j == nkv - 1) {
@@ -633,7 +673,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
           }
           if (lane == 0) {
             mma_commit(&bar_empty[vs]);
-            if (has_next) {
+            if (!kSepP && has_next) {
               if (j + 1 >= nkv) mbar_wait(&bar_full[ks], (ki / NS) & 1, abort, p.status, kSiteMmaFull);
               mma_commit(&bar_empty[ks]);
             }
@@ -686,7 +726,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         mbar_wait(&bar_s[g], tcnt & 1, abort, p.status, kSiteSoftmaxS);
         __syncwarp();  // lanes leave the wait at different times; tcgen05.ld is warp-collective
         if (!live) {
-          if constexpr (kHalfP) mbar_arrive(&bar_ph[g]);
+          if constexpr (kSepP) {
+            mbar_arrive(&bar_sfree[g]);
+            // The next S can be ready before the live warps release this tile's P; arriving on
+            // bar_p only once the previous tile's P V is done keeps this warp's arrivals in the
+            // phase of the tile they belong to.
+            if (j > 0) mbar_wait(&bar_pv[g], (tcnt - 1) & 1, abort, p.status, kSiteSoftmaxPV);
+          }
           mbar_arrive(&bar_p[g]);
           continue;
         }
@@ -717,22 +763,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         tmem_ld_wait(sr + 32);
         tmem_ld_wait(sr + 64);
         tmem_ld_wait(sr + 96);
+        if constexpr (kSepP) {
+          tc_fence_before();
+          mbar_arrive(&bar_sfree[g]);  // S is in registers: the next tile's Q K^T may overwrite it
+        }
         const float m_tile = row_max_chunks<0, 4>(sr) * sl2;
         const bool need = m_tile > m_run + kRescaleThreshold;
         const float alpha = need ? ex2(m_run - m_tile) : 1.f;  // 0 while m_run is -inf
         if (need) m_run = m_tile;
         const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
         float la, lb;
-        if constexpr (kHalfP) {
-          split_f32x2(softmax_chunks<0, 2>(sr, sl2, neg_m, tS), la, lb);
+        if constexpr (kSepP) {
+          uint32_t pk[kBN / 2];
+          split_f32x2(softmax_regs(sr, sl2, neg_m, pk), la, lb);
+          if (j > 0) {
+            // the previous tile's P V must have read P and written O
+            mbar_wait(&bar_pv[g], (tcnt - 1) & 1, abort, p.status, kSiteSoftmaxPV);
+            __syncwarp();
+            tc_fence_after();
+          }
           rescale_o<D>(tO, j > 0 && __any_sync(0xffffffffu, need), alpha);
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&bar_ph[g]);  // keys 0-63 of P (and the rescaled O) are in TMEM
-          float lc, ld;
-          split_f32x2(softmax_chunks<2, 2>(sr, sl2, neg_m, tS), lc, ld);
-          la += lc;
-          lb += ld;
+          const uint32_t tP = tmem + kColP + g * 64 + lane_off;
+#pragma unroll
+          for (int cc = 0; cc < kBN / 32; ++cc) tmem_st16(tP + cc * 16, pk + cc * 16);
         } else {
           split_f32x2(softmax_chunks<0, 4>(sr, sl2, neg_m, tS), la, lb);
           // after P is written, so S no longer occupies registers
