@@ -56,8 +56,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one headline prefill launch from an ncu capture, and the kernel
 # state it was taken on (the digest of its sources without comments); the bench reports it as
 # roofline.traffic only while that code is unchanged.
-PREFILL_TRAFFIC = {"bytes": 440078080 + 111696128,
-                   "source_sha256": "6d887834e3f2cb5454d599f65e2b0206e18ad962df6e3f9cfd09356df7c6a9a1"}
+PREFILL_TRAFFIC = {"bytes": 441330176 + 111323392,
+                   "source_sha256": "595a1d26fd9d6f85a1afd1368b7c2ff369a9818aca5e999101406d051b588b66"}
 L2_FLUSH_BYTES = 512 << 20
 
 
