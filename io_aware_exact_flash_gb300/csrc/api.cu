@@ -356,8 +356,11 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
                         int total_q, int max_q_len, int page_size, int max_pages_per_seq, int num_pages, int Hq,
                         int Hkv, int d, int causal, float scale, void* o, float* o_f32, float* lse, void* workspace,
                         size_t workspace_bytes, int num_splits, fa_stream_t stream, float* ext_o_parts = nullptr,
-                        float* ext_lse_parts = nullptr) {
-  if (total_q == 0) return FA_OK;
+                        float* ext_lse_parts = nullptr, cudaEvent_t after_plan = nullptr) {
+  // after_plan: recorded once the pass's planning kernel is queued (or, on a path without one,
+  // before its first launch), so that other streams can start work that must not run ahead of
+  // this pass taking its SMs
+  if (total_q == 0) return after_plan && cudaEventRecord(after_plan, stream) != cudaSuccess ? FA_ERR_CUDA : FA_OK;
   const int group = Hq / Hkv;
 
   if (max_q_len == 1 && !decode_on_tensor_cores(group)) {
@@ -394,6 +397,7 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
     p.heads_per_cta = dp.heads_per_cta;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.status = dev->status;
+    if (after_plan && cudaEventRecord(after_plan, stream) != cudaSuccess) return FA_ERR_CUDA;
     return fa::launch_decode(p, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 
@@ -469,10 +473,10 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
     // one planning item per sequence (at most 32 query rows); the unit's heads are the group
     p.pack = 1;
     if (fa::launch_decode_tc(p, kr_columns, dev->sm_count, prefill_max_items(num_seqs, total_q, pack), cost_buckets,
-                             work_list, work_count, stream) != cudaSuccess)
+                             work_list, work_count, stream, after_plan) != cudaSuccess)
       return FA_ERR_CUDA;
   } else if (fa::launch_prefill_paged(p, d, dev->sm_count, prefill_max_items(num_seqs, total_q, pack), cost_buckets,
-                                      work_list, work_count, stream) != cudaSuccess) {
+                                      work_list, work_count, stream, after_plan) != cudaSuccess) {
     return FA_ERR_CUDA;
   }
   if (kv_splits > 1 && !external &&
@@ -703,20 +707,23 @@ fa_status fa_cascade_fwd(const void* q, const void* k_pages, const void* v_pages
   void* scratch_pre = base + parts;
   void* scratch_suf = base + parts + scratch_a;
   const size_t suf_bytes = workspace_bytes - parts - scratch_a;
-  // the suffix pass runs on a second stream, forked from and joined back into `stream`
+  // The suffix pass runs on a second stream, forked from and joined back into `stream`. The fork
+  // point is the prefix pass's planning kernel: the prefix's attention kernel is then queued before
+  // the suffix's, takes its SMs first and runs beside the suffix pass, which fills the other SMs
+  // and those the prefix frees. (Forked before the prefix's planning, the suffix's persistent grid
+  // could take every SM first and push the prefix pass behind it.)
   const SideStream* side = side_stream();
   cudaStream_t suf_stream = stream;
-  if (side) {
-    if (cudaEventRecord(side->fork, stream) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-      return FA_ERR_CUDA;
-    suf_stream = side->stream;
-  }
   // prefix pass: every query row of a group sees all of the group's shared keys; its key splits
   // (parts 0 .. sp-1) are left for the final merge
   err = enqueue_paged(dev, q, k_pages, v_pages, prefix_page_table, cu_q_groups, prefix_lens, num_groups, total_q,
                       max_group_q_len, page_size, max_prefix_pages, num_pages, Hq, Hkv, d, 0, scale, nullptr, o_parts,
                       lse_parts, scratch_pre, scratch_a, sp, stream, sp > 1 ? o_parts : nullptr,
-                      sp > 1 ? lse_parts : nullptr);
+                      sp > 1 ? lse_parts : nullptr, side ? side->fork : nullptr);
+  if (err == FA_OK && side) {
+    if (cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess) return FA_ERR_CUDA;
+    suf_stream = side->stream;
+  }
   // suffix pass: each sequence's own keys, with the caller's masking (part sp)
   fa_status err_suf = FA_OK;
   if (err == FA_OK)

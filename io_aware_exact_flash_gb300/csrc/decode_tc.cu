@@ -669,8 +669,9 @@ int decode_tc_columns(int max_q_len, int group, int d, int max_rows) {
 }
 
 cudaError_t launch_decode_tc(const PrefillParams& p, int columns, int sm_count, int max_items, int max_kv_tiles,
-                             int2* work_list, int* work_count, cudaStream_t stream) {
+                             int2* work_list, int* work_count, cudaStream_t stream, cudaEvent_t after_plan) {
   cudaError_t e = launch_plan_paged(p, max_items, max_kv_tiles, work_list, work_count, stream);
+  if (e == cudaSuccess && after_plan != nullptr) e = cudaEventRecord(after_plan, stream);
   if (e != cudaSuccess) return e;
   const long long units = (long long)max_items * p.Hkv * p.kv_splits;  // an upper bound
   const int grid = (int)(units < sm_count ? units : sm_count);

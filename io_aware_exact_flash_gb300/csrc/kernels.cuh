@@ -110,8 +110,10 @@ int current_device_info(DeviceStatus** status, int* sm_count);
 // that have not started; with the take-over off, paged work runs on a persistent grid instead
 // (min(units, sm_count) CTAs looping over the units).
 cudaError_t launch_prefill_dense(const PrefillParams& p, int d, int sm_count, cudaStream_t stream);
+// after_plan (optional) is recorded on the stream between the planning kernel and the attention kernel.
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
-                                 int2* work_list, int* work_count, cudaStream_t stream);
+                                 int2* work_list, int* work_count, cudaStream_t stream,
+                                 cudaEvent_t after_plan = nullptr);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 // The paged planning kernel alone: (sequence, tile pair) items longest first into work_list, their
 // count into work_count[0], and work_count[1] = 0 (the unit counter of launch_decode_tc).
@@ -124,7 +126,7 @@ int decode_tc_columns(int max_q_len, int group, int d, int max_rows);
 // Plans the batch (p.pack must be 1 for the plan) and runs it on min(units, sm_count) persistent
 // CTAs. p.tm_q's box is {64, group, 16 / group, 1}.
 cudaError_t launch_decode_tc(const PrefillParams& p, int columns, int sm_count, int max_items, int max_kv_tiles,
-                             int2* work_list, int* work_count, cudaStream_t stream);
+                             int2* work_list, int* work_count, cudaStream_t stream, cudaEvent_t after_plan = nullptr);
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H,
                          int d, void* o, float* o_f32, float* lse, bool log2_domain, cudaStream_t stream);
 

@@ -1089,8 +1089,9 @@ cudaError_t launch_plan_paged(const PrefillParams& p, int max_items, int max_kv_
 }
 
 cudaError_t launch_prefill_paged(const PrefillParams& p, int d, int sm_count, int max_items, int max_kv_tiles,
-                                 int2* work_list, int* work_count, cudaStream_t stream) {
+                                 int2* work_list, int* work_count, cudaStream_t stream, cudaEvent_t after_plan) {
   cudaError_t e = launch_plan_paged(p, max_items, max_kv_tiles, work_list, work_count, stream);
+  if (e == cudaSuccess && after_plan != nullptr) e = cudaEventRecord(after_plan, stream);
   if (e != cudaSuccess) return e;
   const long long units = (long long)max_items * (p.Hq / p.pack) * p.kv_splits;
   const int mode = persistent_override();
