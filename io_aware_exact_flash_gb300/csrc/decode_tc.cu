@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(288, 1) decode_tc_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched while the planning kernel may still run: its work list and unit counter (and so
+  // everything after this point) wait for it to finish
+  griddep_wait();
   const uint32_t tmem = tmem_base_sh;
   volatile int* abort = &abort_flag;
   const int G = p.group;
@@ -653,8 +656,19 @@ cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t
     if (e != cudaSuccess) return e;
     if (dev < 32) configured_mask.fetch_or(1u << dev, std::memory_order_release);
   }
-  kern<<<grid, 288, KrCfg<N>::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the CTAs may start (barrier set-up, TMEM allocation) while
+  // the planning kernel before them runs; they wait for it before reading its results
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(288);
+  cfg.dynamicSmemBytes = KrCfg<N>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace

@@ -911,6 +911,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_paged_kernel(
     int* __restrict__ scratch) {
   extern __shared__ int plan_smem[];  // max_cost + 1 buckets, or (<= nt sequences) 2 * nt ints
   __shared__ int warp_sums[32];
+  // the key-row decode kernel after this one may start its set-up now (it waits for this kernel's
+  // results before reading them)
+  if (threadIdx.x == 0) griddep_launch_dependents();
   __shared__ int total;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5;
   auto cost_in = [&](int s) {
