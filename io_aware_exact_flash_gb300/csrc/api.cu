@@ -480,7 +480,8 @@ fa_status enqueue_paged(const DeviceInfo* dev, const void* q, const void* k_page
     return FA_ERR_CUDA;
   }
   if (kv_splits > 1 && !external &&
-      fa::launch_merge(p.o_part, p.lse_part, kv_splits, total_q, Hq, d, o, o_f32, lse, false, stream) != cudaSuccess)
+      fa::launch_merge(p.o_part, p.lse_part, kv_splits, total_q, Hq, d, o, o_f32, lse, false, stream,
+                       kr_columns > 0) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ o_
                                                     const float* __restrict__ lse_part, int num_parts, int n_rows,
                                                     int H, int D, __nv_bfloat16* __restrict__ o,
                                                     float* __restrict__ o_f32, float* __restrict__ lse) {
+  griddep_wait();  // launched as a programmatic dependent: the partial states must be complete
   const int64_t row = blockIdx.x;
   const int per_head = D / 4;
   const int t = blockIdx.y * blockDim.x + threadIdx.x;
@@ -450,9 +451,25 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
 }
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H, int d, void* o,
-                         float* o_f32, float* lse, bool log2_domain, cudaStream_t stream) {
+                         float* o_f32, float* lse, bool log2_domain, cudaStream_t stream, bool programmatic) {
   auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
   const dim3 grid((unsigned)n_rows, (unsigned)((H * (d / 4) + 127) / 128));
+  if (programmatic) {
+    // the CTAs may be resident before the kernel ahead of them ends; they wait for it first
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return log2_domain ? cudaLaunchKernelEx(&cfg, merge_kernel<true>, o_part, lse_part, num_parts, n_rows, H, d, ob,
+                                            o_f32, lse)
+                       : cudaLaunchKernelEx(&cfg, merge_kernel<false>, o_part, lse_part, num_parts, n_rows, H, d, ob,
+                                            o_f32, lse);
+  }
   if (log2_domain)
     merge_kernel<true><<<grid, 128, 0, stream>>>(o_part, lse_part, num_parts, n_rows, H, d, ob, o_f32, lse);
   else

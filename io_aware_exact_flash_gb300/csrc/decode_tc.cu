@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(288, 1) decode_tc_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // a key-split merge after this kernel may be made resident now; it waits for this kernel
+    griddep_launch_dependents();
     abort_flag = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);

@@ -127,7 +127,10 @@ int decode_tc_columns(int max_q_len, int group, int d, int max_rows);
 // CTAs. p.tm_q's box is {64, group, 16 / group, 1}.
 cudaError_t launch_decode_tc(const PrefillParams& p, int columns, int sm_count, int max_items, int max_kv_tiles,
                              int2* work_list, int* work_count, cudaStream_t stream, cudaEvent_t after_plan = nullptr);
+// programmatic: launched as a programmatic dependent of the kernel before it on the stream (which
+// should signal its dependents early); the merge waits for that kernel before reading.
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int num_parts, int n_rows, int H,
-                         int d, void* o, float* o_f32, float* lse, bool log2_domain, cudaStream_t stream);
+                         int d, void* o, float* o_f32, float* lse, bool log2_domain, cudaStream_t stream,
+                         bool programmatic = false);
 
 }  // namespace fa
