@@ -56,8 +56,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one headline prefill launch from an ncu capture, and the kernel
 # state it was taken on (the digest of its sources without comments); the bench reports it as
 # roofline.traffic only while that code is unchanged.
-PREFILL_TRAFFIC = {"bytes": 441330176 + 111323392,
-                   "source_sha256": "595a1d26fd9d6f85a1afd1368b7c2ff369a9818aca5e999101406d051b588b66"}
+PREFILL_TRAFFIC = {"bytes": 433830656 + 111355136,
+                   "source_sha256": "b436afe8a8638ec6ab6946daf906fa2e835754f64960a86444021467a88257d4"}
 L2_FLUSH_BYTES = 512 << 20
 
 
