@@ -553,7 +553,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     // into lockstep, both softmaxes run at once and the tensor core idles meanwhile. Turns are
     // taken only at the steps where both tiles issue MMAs (the first Q K^T, then every key tile
     // both tiles attend to): both issuers know both tiles' key-tile counts, so they skip the same
-    // steps. A unit with one query tile (decode, verify) then takes no turns at all.
+    // steps. A unit with one query tile (decode, verify) then takes no turns at all. At d = 64
+    // (separate P) the issuers take no turns: each issues a tile's next Q K^T as soon as its S has
+    // been read and its P V as soon as P is written.
     uint32_t turn = 0;
     auto take_turn = [&]() {
       if (g == 0) {
