@@ -141,6 +141,22 @@ def test_key_row_many_key_splits():
     compare(o1, o_ref, lse1, lse_ref, "key rows, 16 key splits", vabs=va_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("splits", [0, 2])
+def test_partly_filled_query_tiles_over_many_key_tiles(d, splits):
+    """Chunks of 1 to 40 tokens at the end of 640 to 2560 keys, one query head per kv head, so a
+    query tile has one or two warps with query rows and two or three without, over 5 to 20 key
+    tiles. At d = 64 a tile's next scores can be ready before its P is released; the warps without
+    rows must still arrive on the P barrier in their own tile's phase, which a wrong order breaks
+    (non-finite or wrong O)."""
+    lengths = [700, 2049, 1500, 640, 2560, 999]
+    q_lens = [1, 17, 33, 40, 9, 31]
+    t = build_case(lengths, 8, 8, d, 64, False, 131 + d + splits, q_lens=q_lens, extra_pages=2)
+    o, lse = run_paged(t, True, 1 / math.sqrt(d), num_splits=splits)
+    o_ref, lse_ref, va_ref = oracle_paged(t, True, 1 / math.sqrt(d))
+    compare(o, o_ref, lse, lse_ref, f"partly filled tiles d={d} splits={splits}", vabs=va_ref)
+
+
 def test_paged_prefill_full_size_sampled():
     """The ragged paged prefill workload (64 sequences, lengths 512..8192) at full size, in the
     benchmark's launch configuration, checked on sampled (token, head) rows."""
