@@ -150,8 +150,9 @@ fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int num_
  * prefix; with causal != 0 the suffix is masked bottom-right, which needs q_len(s) <= kv_lens[s]
  * (the query tokens lie in the suffix). Both passes run the same kernels as fa_paged_fwd with
  * fp32 outputs, then one merge. The suffix pass runs on a second stream of the library's (one per
- * calling host thread and GPU, created on first use), forked from `stream` with an event before
- * the prefix pass and joined back into it before the merge, so the two passes share the GPU: the
+ * calling host thread and GPU, created on first use), forked from `stream` with an event after
+ * the prefix pass's planning kernel and joined back into it before the merge, so the two passes
+ * share the GPU, the prefix pass starting on its SMs first: the
  * call is ordered on `stream` like any other (and can be captured in a CUDA graph from it).
  *   max_group_q_len / max_q_len: host-side bounds of the query rows per group / per sequence.
  *   workspace: at least fa_cascade_workspace_bytes(...) bytes, 256-byte aligned.
