@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(288, 1) decode_tc_kernel(const __grid_constant
 }
 
 template <int R>
-cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t stream, bool programmatic) {
   constexpr int N = 16;
   auto kern = decode_tc_kernel<N, R>;
   static std::atomic<unsigned> configured_mask{0u};  // one bit per device ordinal below 32
@@ -660,6 +660,10 @@ cudaError_t launch_decode_tc_impl(const PrefillParams& p, int grid, cudaStream_t
   }
   // programmatic stream serialization: the CTAs may start (barrier set-up, TMEM allocation) while
   // the planning kernel before them runs; they wait for it before reading its results
+  if (!programmatic) {
+    kern<<<grid, 288, KrCfg<N>::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(288);
@@ -693,9 +697,10 @@ cudaError_t launch_decode_tc(const PrefillParams& p, int columns, int sm_count, 
   const int grid = (int)(units < sm_count ? units : sm_count);
   if (grid <= 0) return cudaSuccess;
   switch (columns) {
-    case 4: return launch_decode_tc_impl<4>(p, grid, stream);
-    case 8: return launch_decode_tc_impl<8>(p, grid, stream);
-    case 16: return launch_decode_tc_impl<16>(p, grid, stream);
+    // with an event recorded between the plan and this kernel, an ordinary launch
+    case 4: return launch_decode_tc_impl<4>(p, grid, stream, after_plan == nullptr);
+    case 8: return launch_decode_tc_impl<8>(p, grid, stream, after_plan == nullptr);
+    case 16: return launch_decode_tc_impl<16>(p, grid, stream, after_plan == nullptr);
     default: return cudaErrorInvalidValue;
   }
 }

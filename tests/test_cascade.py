@@ -119,6 +119,20 @@ def test_cascade_groups_and_chunks(causal, d, Hq, Hkv):
     compare(o, o_ref, lse, lse_ref, f"cascade groups causal={causal} d={d}", vabs=va_ref)
 
 
+def test_cascade_prefix_pass_on_the_key_row_kernel():
+    """Groups of one to four decode rows at group size 4 (at most 16 query rows per kv head), so
+    the prefix pass runs on the key-row decode kernel too, with the cascade's fork event recorded
+    between that pass's planning kernel and its attention kernel."""
+    groups = [4, 3, 1, 2]
+    prefix = [700, 2049, 16, 300]
+    suffix = [1, 5, 16, 17, 100, 300, 2, 64, 129, 1000]
+    c = build(groups, prefix, [1] * len(suffix), suffix, 32, 8, 128, 16, seed=61)
+    scale = 1 / math.sqrt(128)
+    o, lse = run_cascade(c, True, scale)
+    o_ref, lse_ref, va_ref = oracle_flat(c, True, scale)
+    compare(o, o_ref, lse, lse_ref, "cascade, key-row prefix pass", vabs=va_ref)
+
+
 def test_cascade_full_size_decode():
     """128 decode sequences behind one 16384-token prefix (suffixes of 256..2048 tokens): every
     output row against the oracle over the flat layout (the prefix is page aligned, so each
