@@ -40,6 +40,10 @@ struct DecodeCfg {
   static constexpr int CPL = EPL / 8;      // 16-byte chunks per lane
   static constexpr int RPI = 32 / LPR;     // rows a warp handles per step
   static constexpr int ITERS = kRowsPerBlock / RPI;
+  // a block is taken in SUB sub-blocks of SITERS steps (one max / rescale each), so that the
+  // scores held at once (SITERS x G per lane) stay within 16 registers where they would exceed 32
+  static constexpr int SUB = (ITERS * G > 32) ? 4 : 1;
+  static constexpr int SITERS = ITERS / SUB;
 };
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
@@ -164,65 +168,68 @@ __global__ void __launch_bounds__(kMaxHeadsPerCta * 32, 1)
     const uint8_t* sk = smem + (size_t)s * 2 * chunk;
     const uint8_t* sv = sk + chunk;
     const int row_base = (blk_begin + i) * kRowsPerBlock;
-    float sc[C::ITERS][G];
 #pragma unroll
-    for (int it = 0; it < C::ITERS; ++it) {
-      const int r = it * C::RPI + rg;
-      const uint4* kp = reinterpret_cast<const uint4*>(sk + ((size_t)r * hpc + warp) * D * 2);
-      uint64_t kf2[C::EPL / 2];
+    for (int hb = 0; hb < C::SUB; ++hb) {
+      float sc[C::SITERS][G];
 #pragma unroll
-      for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32x2(kp[lr + c * C::LPR], &kf2[c * 4]);
+      for (int it = 0; it < C::SITERS; ++it) {
+        const int r = (hb * C::SITERS + it) * C::RPI + rg;
+        const uint4* kp = reinterpret_cast<const uint4*>(sk + ((size_t)r * hpc + warp) * D * 2);
+        uint64_t kf2[C::EPL / 2];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        uint64_t acc2 = 0ull;
-#pragma unroll
-        for (int e = 0; e < C::EPL / 2; ++e) acc2 = fma_f32x2(qf2[g][e], kf2[e], acc2);
-        float a0, a1;
-        split_f32x2(acc2, a0, a1);
-        float acc = a0 + a1;
-#pragma unroll
-        for (int sh = 1; sh < C::LPR; sh <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-        sc[it][g] = (row_base + r < kv_len) ? acc : -INFINITY;
-      }
-    }
-    // one max / rescale per block of 16 rows
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float bm = sc[0][g];
-#pragma unroll
-      for (int it = 1; it < C::ITERS; ++it) bm = fmaxf(bm, sc[it][g]);
-#pragma unroll
-      for (int sh = C::LPR; sh < 32; sh <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, sh));
-      const float m_new = fmaxf(m[g], bm);
-      if (m_new > m[g]) {
-        const float alpha = ex2(m[g] - m_new);  // 0 while m is -inf
-        l[g] *= alpha;
-        const uint64_t a2 = f32x2(alpha, alpha);
-#pragma unroll
-        for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = mul_f32x2(o2[g][e], a2);
-        m[g] = m_new;
-      }
-      const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
-#pragma unroll
-      for (int it = 0; it < C::ITERS; ++it) {
-        sc[it][g] = ex2(sc[it][g] - mu);
-        l[g] += sc[it][g];
-      }
-    }
-#pragma unroll
-    for (int it = 0; it < C::ITERS; ++it) {
-      const int r = it * C::RPI + rg;
-      const uint4* vp = reinterpret_cast<const uint4*>(sv + ((size_t)r * hpc + warp) * D * 2);
-      uint64_t vf2[C::EPL / 2];
-#pragma unroll
-      for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32x2(vp[lr + c * C::LPR], &vf2[c * 4]);
-      // rows past kv_len carry p = 0; their V may be arbitrary bits, so they are skipped
-      if (row_base + r < kv_len) {
+        for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32x2(kp[lr + c * C::LPR], &kf2[c * 4]);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const uint64_t p2 = f32x2(sc[it][g], sc[it][g]);
+          uint64_t acc2 = 0ull;
 #pragma unroll
-          for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = fma_f32x2(p2, vf2[e], o2[g][e]);
+          for (int e = 0; e < C::EPL / 2; ++e) acc2 = fma_f32x2(qf2[g][e], kf2[e], acc2);
+          float a0, a1;
+          split_f32x2(acc2, a0, a1);
+          float acc = a0 + a1;
+#pragma unroll
+          for (int sh = 1; sh < C::LPR; sh <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+          sc[it][g] = (row_base + r < kv_len) ? acc : -INFINITY;
+        }
+      }
+      // one max / rescale per sub-block
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float bm = sc[0][g];
+#pragma unroll
+        for (int it = 1; it < C::SITERS; ++it) bm = fmaxf(bm, sc[it][g]);
+#pragma unroll
+        for (int sh = C::LPR; sh < 32; sh <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, sh));
+        const float m_new = fmaxf(m[g], bm);
+        if (m_new > m[g]) {
+          const float alpha = ex2(m[g] - m_new);  // 0 while m is -inf
+          l[g] *= alpha;
+          const uint64_t a2 = f32x2(alpha, alpha);
+#pragma unroll
+          for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = mul_f32x2(o2[g][e], a2);
+          m[g] = m_new;
+        }
+        const float mu = (m[g] == -INFINITY) ? 0.f : m[g];
+#pragma unroll
+        for (int it = 0; it < C::SITERS; ++it) {
+          sc[it][g] = ex2(sc[it][g] - mu);
+          l[g] += sc[it][g];
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < C::SITERS; ++it) {
+        const int r = (hb * C::SITERS + it) * C::RPI + rg;
+        const uint4* vp = reinterpret_cast<const uint4*>(sv + ((size_t)r * hpc + warp) * D * 2);
+        uint64_t vf2[C::EPL / 2];
+#pragma unroll
+        for (int c = 0; c < C::CPL; ++c) bf16x8_to_f32x2(vp[lr + c * C::LPR], &vf2[c * 4]);
+        // rows past kv_len carry p = 0; their V may be arbitrary bits, so they are skipped
+        if (row_base + r < kv_len) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const uint64_t p2 = f32x2(sc[it][g], sc[it][g]);
+#pragma unroll
+            for (int e = 0; e < C::EPL / 2; ++e) o2[g][e] = fma_f32x2(p2, vf2[e], o2[g][e]);
+          }
         }
       }
     }
